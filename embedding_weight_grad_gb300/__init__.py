@@ -1,0 +1,230 @@
+"""Sparse embedding weight-gradient accumulation on GB300 (sm_103a).
+
+``accumulate_embedding_wgrad(ids, grad, main_grad)`` performs
+``main_grad += embedding_dense_backward(grad, ids)`` touching only the rows of the ids
+that occur, with the values of PyTorch's sort-based embedding backward followed by
+``main_grad.add_`` (Megatron Core API docs, ``core.fusions.fused_embedding_wgrad``:
+module docstring, ``accumulate_embedding_wgrad`` and ``can_accumulate_embedding_wgrad``).
+
+This module only marshals arguments into the C ABI of ``libewg.so`` (declared in
+``include/ewg.h``); every step of the computation runs in that library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no CPU
+fallback: without the compiled library every entry point raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "MIN_TOKENS", "MAX_TOKENS", "NROWS", "EwgError", "can_accumulate_embedding_wgrad",
+    "accumulate_embedding_wgrad", "workspace_bytes", "plan", "apply", "read_status",
+    "library_path", "lib",
+]
+
+MIN_TOKENS = 3073
+MAX_TOKENS = 1 << 28
+NROWS = 10
+
+_INT32, _INT64, _BF16, _FP32 = 0, 1, 2, 3
+OK, ERR_UNSUPPORTED, ERR_INVALID, ERR_CUDA, ERR_ID_OUT_OF_RANGE = 0, 1, 2, 3, 4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libewg.so")
+_lib = None
+_lock = threading.Lock()
+
+
+class EwgError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(msg)
+        self.code = code
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded C library; raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(
+                    f"{_LIB_PATH} is missing: build it with "
+                    "`python -m embedding_weight_grad_gb300.build` (needs nvcc)")
+            L = ctypes.CDLL(_LIB_PATH)
+            i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            L.ewg_can_accumulate.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64]
+            L.ewg_can_accumulate.restype = i32
+            L.ewg_workspace_bytes.argtypes = [i64, i64]
+            L.ewg_workspace_bytes.restype = sz
+            L.ewg_accumulate.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64, vp,
+                                         sz, vp]
+            L.ewg_accumulate.restype = i32
+            L.ewg_plan.argtypes = [vp, i32, i64, i64, i64, vp, sz, vp]
+            L.ewg_plan.restype = i32
+            L.ewg_apply.argtypes = [vp, i32, i64, vp, i32, i64, i64, i64, i64, vp, sz, vp]
+            L.ewg_apply.restype = i32
+            L.ewg_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+            L.ewg_read_status.restype = i32
+            L.ewg_status_string.argtypes = [i32]
+            L.ewg_status_string.restype = ctypes.c_char_p
+            L.ewg_last_error.argtypes = []
+            L.ewg_last_error.restype = ctypes.c_char_p
+            L.ewg_version.argtypes = []
+            L.ewg_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def _raise_on(code: int):
+    if code != OK:
+        L = lib()
+        raise EwgError(code, f"{L.ewg_status_string(code).decode()}: {L.ewg_last_error().decode()}")
+
+
+_FLOAT_CODES = {torch.bfloat16: _BF16, torch.float32: _FP32}
+_ID_CODES = {torch.int32: _INT32, torch.int64: _INT64}
+
+
+def _stream_ptr(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+class _Args:
+    """The C-ABI view of (ids, grad, main_grad), or the reason there is none."""
+
+    def __init__(self, ids: torch.Tensor, grad: torch.Tensor, main_grad: torch.Tensor):
+        self.reason = None
+        if not (ids.is_cuda and grad.is_cuda and main_grad.is_cuda):
+            self.reason = "tensors must be on a CUDA device"
+            return
+        if ids.dtype not in _ID_CODES or grad.dtype not in _FLOAT_CODES \
+                or main_grad.dtype not in _FLOAT_CODES:
+            self.reason = "ids must be int32/int64; grad and main_grad bf16/fp32"
+            return
+        if main_grad.dim() != 2 or main_grad.stride(1) != 1:
+            self.reason = "main_grad must be [num_embeddings, hidden] with unit inner stride"
+            return
+        if not ids.is_contiguous():
+            self.reason = "ids must be contiguous"
+            return
+        V, H = main_grad.shape
+        n = ids.numel()
+        if tuple(grad.shape) != tuple(ids.shape) + (H,):
+            self.reason = "grad must be [*ids.shape, hidden]"
+            return
+        try:
+            g2 = grad.view(n, H)
+        except RuntimeError:
+            self.reason = "grad rows must share one row stride"
+            return
+        if H > 0 and n > 0 and g2.stride(1) != 1:
+            self.reason = "grad must have unit inner stride"
+            return
+        self.ids, self.grad, self.main_grad = ids.reshape(n), g2, main_grad
+        self.n, self.V, self.H = n, V, H
+        self.grad_stride = g2.stride(0) if n > 1 else H
+        self.mg_stride = main_grad.stride(0) if V > 1 else H
+        self.device = main_grad.device
+
+    def c_args(self):
+        return (self.ids.data_ptr(), _ID_CODES[self.ids.dtype], self.n,
+                self.grad.data_ptr(), _FLOAT_CODES[self.grad.dtype], self.grad_stride,
+                self.main_grad.data_ptr(), _FLOAT_CODES[self.main_grad.dtype], self.V, self.H,
+                self.mg_stride)
+
+
+def can_accumulate_embedding_wgrad(ids: torch.Tensor, grad: torch.Tensor,
+                                   main_grad: torch.Tensor) -> bool:
+    """Whether accumulate_embedding_wgrad supports these tensors (see include/ewg.h)."""
+    a = _Args(ids, grad, main_grad)
+    if a.reason is not None:
+        return False
+    with torch.cuda.device(a.device):
+        return bool(lib().ewg_can_accumulate(*a.c_args()))
+
+
+def workspace_bytes(num_tokens: int, hidden: int) -> int:
+    return int(lib().ewg_workspace_bytes(num_tokens, hidden))
+
+
+def new_workspace(num_tokens: int, hidden: int, device=None) -> torch.Tensor:
+    """A device buffer large enough for any call with these sizes (no init needed)."""
+    nbytes = workspace_bytes(num_tokens, hidden)
+    if nbytes == 0:
+        raise EwgError(ERR_UNSUPPORTED, "unsupported num_tokens / hidden")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def accumulate_embedding_wgrad(ids: torch.Tensor, grad: torch.Tensor, main_grad: torch.Tensor,
+                               *, workspace: torch.Tensor | None = None,
+                               check: bool = False) -> None:
+    """main_grad += embedding_dense_backward(grad, ids), touching only the rows of ids.
+
+    ids: token ids, any shape, num_tokens elements; grad: [*ids.shape, hidden];
+    main_grad: [num_embeddings, hidden], updated in place.  Requires
+    can_accumulate_embedding_wgrad(ids, grad, main_grad) (raises ValueError otherwise).
+    The work is enqueued on the current stream.  With check=True the call waits for it
+    and raises EwgError if the device found an id outside [0, num_embeddings), in which
+    case main_grad was left untouched.
+    """
+    a = _Args(ids, grad, main_grad)
+    if a.reason is not None:
+        raise ValueError(f"accumulate_embedding_wgrad does not support these tensors: {a.reason}")
+    with torch.cuda.device(a.device):
+        L = lib()
+        if not L.ewg_can_accumulate(*a.c_args()):
+            raise ValueError("accumulate_embedding_wgrad does not support these tensors: "
+                             + L.ewg_last_error().decode())
+        ws = workspace if workspace is not None else new_workspace(a.n, a.H, a.device)
+        stream = _stream_ptr(a.device)
+        _raise_on(L.ewg_accumulate(*a.c_args(), ws.data_ptr(), ws.numel(), stream))
+        if check:
+            raise_on_device_status(ws)
+
+
+def read_status(workspace: torch.Tensor) -> int:
+    """Waits for the current stream and returns the device status of the last call."""
+    status = ctypes.c_int(-1)
+    with torch.cuda.device(workspace.device):
+        _raise_on(lib().ewg_read_status(workspace.data_ptr(), _stream_ptr(workspace.device),
+                                        ctypes.byref(status)))
+    return status.value
+
+
+def raise_on_device_status(workspace: torch.Tensor) -> None:
+    s = read_status(workspace)
+    if s != OK:
+        raise EwgError(s, f"device reported {lib().ewg_status_string(s).decode()}")
+
+
+def plan(ids: torch.Tensor, num_embeddings: int, hidden: int, workspace: torch.Tensor) -> None:
+    """Sort + run listing of ids into `workspace` (first half of the accumulation)."""
+    ids_flat = ids.reshape(-1)
+    if ids.dtype not in _ID_CODES or not ids.is_contiguous():
+        raise ValueError("ids must be contiguous int32/int64")
+    with torch.cuda.device(ids.device):
+        _raise_on(lib().ewg_plan(ids_flat.data_ptr(), _ID_CODES[ids.dtype], ids_flat.numel(),
+                                 num_embeddings, hidden, workspace.data_ptr(), workspace.numel(),
+                                 _stream_ptr(ids.device)))
+
+
+def apply(grad: torch.Tensor, main_grad: torch.Tensor, num_tokens: int,
+          workspace: torch.Tensor) -> None:
+    """Partial sums and the add into main_grad, using the plan in `workspace`."""
+    V, H = main_grad.shape
+    g2 = grad.view(num_tokens, H)
+    with torch.cuda.device(main_grad.device):
+        _raise_on(lib().ewg_apply(g2.data_ptr(), _FLOAT_CODES[grad.dtype],
+                                  g2.stride(0) if num_tokens > 1 else H, main_grad.data_ptr(),
+                                  _FLOAT_CODES[main_grad.dtype], num_tokens, V, H,
+                                  main_grad.stride(0) if V > 1 else H, workspace.data_ptr(),
+                                  workspace.numel(), _stream_ptr(main_grad.device)))

@@ -1,0 +1,296 @@
+// C ABI of the library: argument checks, workspace layout and kernel launches.
+// The declarations and their contracts are in include/ewg.h.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "ewg.h"
+#include "ewg_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(EWG_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_devices[kMaxDevices];
+
+// SM count of the current device; configures the kernels once per device.
+int current_device(int* dev, int* num_sms) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(EWG_ERR_CUDA, "device index out of range");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_devices[*dev];
+  if (!d.ready) {
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, *dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = ewg::prepare_plan_kernels();
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+    d.ready = true;
+  }
+  *num_sms = d.num_sms;
+  return EWG_OK;
+}
+
+bool on_device(const void* p, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of a foreign pointer
+    return false;
+  }
+  return (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) && at.device == dev;
+}
+
+size_t elem_size(int dtype) {
+  switch (dtype) {
+    case EWG_INT32: return 4;
+    case EWG_INT64: return 8;
+    case EWG_BF16: return 2;
+    case EWG_FP32: return 4;
+    default: return 0;
+  }
+}
+
+bool aligned(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+struct Range {
+  uintptr_t lo, hi;
+};
+
+Range span(const void* p, int64_t rows, int64_t cols, int64_t row_stride, size_t es) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  const uintptr_t bytes = rows > 0 ? (static_cast<uintptr_t>(rows - 1) * row_stride + cols) * es : 0;
+  return {lo, lo + bytes};
+}
+
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+int check_sizes(int64_t n, int64_t V, int64_t H) {
+  if (n < EWG_MIN_TOKENS || n > EWG_MAX_TOKENS)
+    return fail(EWG_ERR_UNSUPPORTED, "num_tokens outside [EWG_MIN_TOKENS, EWG_MAX_TOKENS]");
+  if (V < 1 || V > INT32_MAX) return fail(EWG_ERR_UNSUPPORTED, "num_embeddings outside [1, 2^31)");
+  if (H < 8 || H > EWG_MAX_HIDDEN || H % 8 != 0)
+    return fail(EWG_ERR_UNSUPPORTED, "hidden must be a multiple of 8 in [8, EWG_MAX_HIDDEN]");
+  return EWG_OK;
+}
+
+int check_ids(const void* ids, int ids_dtype, int dev) {
+  if (ids_dtype != EWG_INT32 && ids_dtype != EWG_INT64)
+    return fail(EWG_ERR_UNSUPPORTED, "ids must be int32 or int64");
+  if (!ids || !aligned(ids, elem_size(ids_dtype)))
+    return fail(EWG_ERR_UNSUPPORTED, "ids pointer is null or misaligned");
+  if (!on_device(ids, dev)) return fail(EWG_ERR_UNSUPPORTED, "ids is not memory of the current device");
+  return EWG_OK;
+}
+
+int check_mat(const void* p, int dtype, int64_t stride, int64_t H, int dev, const char* name) {
+  if (dtype != EWG_BF16 && dtype != EWG_FP32)
+    return fail(EWG_ERR_UNSUPPORTED, std::string(name) + " must be bf16 or fp32");
+  if (!p || !aligned(p, 16)) return fail(EWG_ERR_UNSUPPORTED, std::string(name) + " is null or not 16-byte aligned");
+  if (stride < H || (stride * static_cast<int64_t>(elem_size(dtype))) % 16 != 0)
+    return fail(EWG_ERR_UNSUPPORTED, std::string(name) + " row stride must be >= hidden and a multiple of 16 bytes");
+  if (!on_device(p, dev)) return fail(EWG_ERR_UNSUPPORTED, std::string(name) + " is not memory of the current device");
+  return EWG_OK;
+}
+
+int check_all(const void* ids, int ids_dtype, int64_t n, const void* grad, int grad_dtype,
+              int64_t grad_row_stride, const void* mg, int mg_dtype, int64_t V, int64_t H,
+              int64_t mg_row_stride, int dev) {
+  int rc = check_sizes(n, V, H);
+  if (rc) return rc;
+  if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
+  if ((rc = check_mat(grad, grad_dtype, grad_row_stride, H, dev, "grad"))) return rc;
+  if ((rc = check_mat(mg, mg_dtype, mg_row_stride, H, dev, "main_grad"))) return rc;
+  const Range rm = span(mg, V, H, mg_row_stride, elem_size(mg_dtype));
+  if (overlap(rm, span(grad, n, H, grad_row_stride, elem_size(grad_dtype))) ||
+      overlap(rm, span(ids, 1, n, n, elem_size(ids_dtype))))
+    return fail(EWG_ERR_UNSUPPORTED, "main_grad overlaps grad or ids");
+  return EWG_OK;
+}
+
+int check_workspace(void* ws, size_t bytes, int64_t n, int64_t H, int dev) {
+  if (!ws || !aligned(ws, 256)) return fail(EWG_ERR_INVALID, "workspace is null or not 256-byte aligned");
+  const size_t need = ewg::make_layout(n, H).total;
+  if (bytes < need)
+    return fail(EWG_ERR_INVALID, "workspace smaller than ewg_workspace_bytes(num_tokens, hidden)");
+  if (!on_device(ws, dev)) return fail(EWG_ERR_INVALID, "workspace is not memory of the current device");
+  return EWG_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t H, void* ws,
+            int num_sms, cudaStream_t stream) {
+  const ewg::Layout L = ewg::make_layout(n, H);
+  const ewg::SortPlan sp = ewg::make_sort_plan(V);
+  ewg::PlanArgs a{};
+  a.ids = ids;
+  a.ids_int64 = ids_dtype == EWG_INT64;
+  a.n = static_cast<int>(n);
+  a.num_embeddings = V;
+  a.hidden = static_cast<int>(H);
+  a.slices = static_cast<int>(L.slices);
+  a.id_bits = sp.id_bits;
+  a.passes = sp.passes;
+  a.digit_bits = sp.digit_bits;
+  a.tiles = static_cast<int>(L.tiles);
+  a.header = at<ewg::Header>(ws, L.header);
+  a.keys_a = at<uint32_t>(ws, L.keys_a);
+  a.vals_a = at<uint32_t>(ws, L.vals_a);
+  a.keys_b = at<uint32_t>(ws, L.keys_b);
+  a.vals_b = at<uint32_t>(ws, L.vals_b);
+  a.chunks = at<int>(ws, L.chunks);
+  a.hist = at<uint32_t>(ws, L.hist);
+  a.tile_bad = at<int>(ws, L.tile_bad);
+  a.tile_cnt = at<long long>(ws, L.tile_cnt);
+  a.counters = at<int>(ws, L.counters);
+  cudaError_t e = ewg::launch_plan(a, num_sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  return EWG_OK;
+}
+
+int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg, int mg_dtype,
+             int64_t n, int64_t V, int64_t H, int64_t mg_row_stride, void* ws, int num_sms,
+             cudaStream_t stream) {
+  const ewg::Layout L = ewg::make_layout(n, H);
+  ewg::ApplyArgs a{};
+  a.grad = grad;
+  a.grad_stride = grad_row_stride;
+  a.main_grad = mg;
+  a.mg_stride = mg_row_stride;
+  a.n = static_cast<int>(n);
+  a.hidden = static_cast<int>(H);
+  a.num_embeddings = V;
+  a.slices = static_cast<int>(L.slices);
+  a.header = at<ewg::Header>(ws, L.header);
+  a.chunks = at<int>(ws, L.chunks);
+  a.counters = at<int>(ws, L.counters);
+  a.partial = at<float>(ws, L.partial);
+  cudaError_t e = ewg::launch_apply(a, grad_dtype == EWG_BF16, mg_dtype == EWG_BF16, num_sms, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "apply launch");
+  return EWG_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ewg_can_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const void* grad,
+                       int grad_dtype, int64_t grad_row_stride, const void* main_grad,
+                       int main_grad_dtype, int64_t num_embeddings, int64_t hidden,
+                       int64_t main_grad_row_stride) {
+  int dev = 0, sms = 0;
+  if (current_device(&dev, &sms) != EWG_OK) return 0;
+  return check_all(ids, ids_dtype, num_tokens, grad, grad_dtype, grad_row_stride, main_grad,
+                   main_grad_dtype, num_embeddings, hidden, main_grad_row_stride, dev) == EWG_OK;
+}
+
+size_t ewg_workspace_bytes(int64_t num_tokens, int64_t hidden) {
+  if (num_tokens < 1 || num_tokens > EWG_MAX_TOKENS || hidden < 8 || hidden > EWG_MAX_HIDDEN ||
+      hidden % 8 != 0)
+    return 0;
+  return ewg::make_layout(num_tokens, hidden).total;
+}
+
+int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const void* grad,
+                   int grad_dtype, int64_t grad_row_stride, void* main_grad, int main_grad_dtype,
+                   int64_t num_embeddings, int64_t hidden, int64_t main_grad_row_stride,
+                   void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  int dev = 0, sms = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  rc = check_all(ids, ids_dtype, num_tokens, grad, grad_dtype, grad_row_stride, main_grad,
+                 main_grad_dtype, num_embeddings, hidden, main_grad_row_stride, dev);
+  if (rc) return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, sms, s);
+  if (rc) return rc;
+  return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
+                  num_embeddings, hidden, main_grad_row_stride, workspace, sms, s);
+}
+
+int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_embeddings,
+             int64_t hidden, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  int dev = 0, sms = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
+  if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  return do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, sms,
+                 static_cast<cudaStream_t>(stream));
+}
+
+int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* main_grad,
+              int main_grad_dtype, int64_t num_tokens, int64_t num_embeddings, int64_t hidden,
+              int64_t main_grad_row_stride, void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  int dev = 0, sms = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
+  if ((rc = check_mat(grad, grad_dtype, grad_row_stride, hidden, dev, "grad"))) return rc;
+  if ((rc = check_mat(main_grad, main_grad_dtype, main_grad_row_stride, hidden, dev, "main_grad")))
+    return rc;
+  if (overlap(span(main_grad, num_embeddings, hidden, main_grad_row_stride, elem_size(main_grad_dtype)),
+              span(grad, num_tokens, hidden, grad_row_stride, elem_size(grad_dtype))))
+    return fail(EWG_ERR_UNSUPPORTED, "main_grad overlaps grad");
+  if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
+                  num_embeddings, hidden, main_grad_row_stride, workspace, sms,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int ewg_read_status(const void* workspace, void* stream, int* status) {
+  g_last_error.clear();
+  if (!workspace || !status) return fail(EWG_ERR_INVALID, "null workspace or status pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const ewg::Header* h = static_cast<const ewg::Header*>(workspace);
+  int v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, &h->status, sizeof v, cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return cuda_fail(e, "status copy");
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  *status = v;
+  return EWG_OK;
+}
+
+const char* ewg_status_string(int status) {
+  switch (status) {
+    case EWG_OK: return "EWG_OK";
+    case EWG_ERR_UNSUPPORTED: return "EWG_ERR_UNSUPPORTED";
+    case EWG_ERR_INVALID: return "EWG_ERR_INVALID";
+    case EWG_ERR_CUDA: return "EWG_ERR_CUDA";
+    case EWG_ERR_ID_OUT_OF_RANGE: return "EWG_ERR_ID_OUT_OF_RANGE";
+    default: return "EWG_ERR_UNKNOWN";
+  }
+}
+
+const char* ewg_last_error(void) { return g_last_error.c_str(); }
+
+int ewg_version(void) { return 1; }
+
+}  // extern "C"

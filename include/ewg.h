@@ -1,0 +1,166 @@
+/*
+ * ewg.h -- C ABI of the GB300 sparse embedding weight-gradient library.
+ *
+ * The operation (Megatron Core API docs, core.fusions.fused_embedding_wgrad,
+ * entry accumulate_embedding_wgrad, and the module docstring):
+ *
+ *     main_grad += embedding_dense_backward(grad, ids)
+ *
+ * touching only the rows of the ids that occur.  The values are those of PyTorch's
+ * sort-based embedding backward followed by main_grad.add_ (module docstring,
+ * both bullets): the (token, position) pairs are sorted; each token's gradient rows
+ * are summed in position order into fp32 partial sums of at most EWG_NROWS rows,
+ * chunked from the token's first row; the partial sums are added in order starting
+ * from 0; the total is rounded once to the gradient dtype; that value is added to
+ * the main_grad row in fp32 and rounded to main_grad's dtype.  Rows of ids that do
+ * not occur are neither read nor written (module docstring, last sentence).
+ * Every rounding is IEEE round-to-nearest-even; results are deterministic and
+ * independent of the launch configuration.
+ *
+ * Conventions for every entry point below:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them.  All tensors must live on the current
+ *     CUDA device.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Work is enqueued on it and the call returns without waiting for it.
+ *   - Errors a host check can find are returned BEFORE anything is enqueued, so
+ *     main_grad is untouched.  Errors found on the device (an id outside
+ *     [0, num_embeddings)) make every kernel of the call skip all writes to
+ *     main_grad; ewg_read_status() reports them.
+ *   - No C++ exception crosses this boundary.  Entry points are thread-safe; two
+ *     calls that share a workspace or a main_grad must be ordered by the caller
+ *     (same stream, or events).
+ */
+#ifndef EWG_H_
+#define EWG_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fewest tokens accepted: PyTorch's embedding backward takes its sort-based path,
+ * whose arithmetic this library reproduces, only above 3072 tokens (module
+ * docstring, first bullet; MIN_TOKENS = 3073 on the same page). */
+#define EWG_MIN_TOKENS 3073
+/* Most tokens accepted.  The page's own limit is 8192 (MAX_TOKENS), set by its
+ * single-program sort; this library sorts across many CTAs and keeps 32-bit slot
+ * indices, so it accepts up to 2^28 tokens. */
+#define EWG_MAX_TOKENS (1 << 28)
+/* Partial-sum chunk length (NROWS on the page, NROWS_PER_THREAD in PyTorch). */
+#define EWG_NROWS 10
+/* Largest hidden size accepted. */
+#define EWG_MAX_HIDDEN (1 << 24)
+
+/* Element types (ewg_dtype). */
+#define EWG_INT32 0
+#define EWG_INT64 1
+#define EWG_BF16 2
+#define EWG_FP32 3
+
+/* Status codes (ewg_status). */
+#define EWG_OK 0
+#define EWG_ERR_UNSUPPORTED 1     /* tensors outside what ewg_can_accumulate accepts */
+#define EWG_ERR_INVALID 2         /* bad argument: NULL, size, workspace too small, plan mismatch */
+#define EWG_ERR_CUDA 3            /* a CUDA runtime call or kernel launch failed */
+#define EWG_ERR_ID_OUT_OF_RANGE 4 /* device-detected: an id outside [0, num_embeddings) */
+
+/*
+ * Whether ewg_accumulate supports these tensors (can_accumulate_embedding_wgrad on
+ * the page).  Returns 1 or 0 and never enqueues work.
+ *
+ *   ids        [num_tokens] contiguous, ids_dtype EWG_INT32 or EWG_INT64.  A
+ *              multi-dimensional ids tensor is passed flattened in row-major order;
+ *              token position p is its flat index.
+ *   grad       [num_tokens][hidden], grad_dtype EWG_BF16 or EWG_FP32, unit inner
+ *              stride, grad_row_stride elements between rows (>= hidden).
+ *   main_grad  [num_embeddings][hidden], EWG_BF16 or EWG_FP32, unit inner stride,
+ *              main_grad_row_stride elements between rows (>= hidden).
+ *
+ * Conditions: EWG_MIN_TOKENS <= num_tokens <= EWG_MAX_TOKENS;
+ * 1 <= num_embeddings < 2^31; 8 <= hidden <= EWG_MAX_HIDDEN and hidden % 8 == 0;
+ * grad, main_grad and their row strides 16-byte aligned; ids aligned to its element;
+ * all three pointers are device (or managed) memory of the current device;
+ * main_grad does not overlap grad or ids.  The page's further conditions (Triton
+ * present, ids and positions packing into 31 bits, at most 8192 tokens) belong to
+ * its own implementation and are not imposed here.
+ */
+int ewg_can_accumulate(const void* ids, int ids_dtype, int64_t num_tokens,
+                       const void* grad, int grad_dtype, int64_t grad_row_stride,
+                       const void* main_grad, int main_grad_dtype,
+                       int64_t num_embeddings, int64_t hidden,
+                       int64_t main_grad_row_stride);
+
+/*
+ * Bytes of device workspace that ewg_accumulate / ewg_plan / ewg_apply need for
+ * num_tokens tokens of width hidden (an upper bound over every id pattern).  The
+ * workspace needs no initialisation and holds no state the caller must keep
+ * between calls, except that ewg_apply reads the plan that ewg_plan left in it and
+ * ewg_read_status reads the status of the last call.  Returns 0 for sizes outside
+ * the supported range.
+ */
+size_t ewg_workspace_bytes(int64_t num_tokens, int64_t hidden);
+
+/*
+ * main_grad += embedding_dense_backward(grad, ids), touching only the rows of ids
+ * (accumulate_embedding_wgrad on the page).  Arguments as for ewg_can_accumulate,
+ * plus a device workspace of at least ewg_workspace_bytes(num_tokens, hidden)
+ * bytes, 256-byte aligned, and the stream.  Equivalent to ewg_plan followed by
+ * ewg_apply on the same stream.
+ *
+ * Returns EWG_OK once the work is enqueued, EWG_ERR_UNSUPPORTED /
+ * EWG_ERR_INVALID (nothing enqueued, main_grad untouched) or EWG_ERR_CUDA.
+ * Out-of-range ids are found on the device: main_grad is then left untouched and
+ * ewg_read_status returns EWG_ERR_ID_OUT_OF_RANGE.
+ */
+int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens,
+                   const void* grad, int grad_dtype, int64_t grad_row_stride,
+                   void* main_grad, int main_grad_dtype,
+                   int64_t num_embeddings, int64_t hidden, int64_t main_grad_row_stride,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The first half of ewg_accumulate (the page's _sort_tokens_kernel): validates the
+ * ids on the device, sorts the (token, position) pairs, finds every token's run of
+ * sorted slots and lists its chunks of at most EWG_NROWS rows, writing this plan
+ * into the workspace.  Reads only ids; writes only the workspace.
+ */
+int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_embeddings,
+             int64_t hidden, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The second half of ewg_accumulate (the page's _partial_sums_kernel and
+ * _long_run_sums_kernel, as one kernel): sums the chunks of the plan in the
+ * workspace and adds each token's row into main_grad.  num_tokens, num_embeddings
+ * and hidden must be those given to the ewg_plan that filled the workspace (the
+ * kernel checks them against the plan and writes nothing on a mismatch, reporting
+ * EWG_ERR_INVALID through ewg_read_status).  Must be ordered after that ewg_plan.
+ */
+int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride,
+              void* main_grad, int main_grad_dtype, int64_t num_tokens,
+              int64_t num_embeddings, int64_t hidden, int64_t main_grad_row_stride,
+              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Waits for `stream`, then copies the device status of the last ewg_plan /
+ * ewg_apply / ewg_accumulate that used this workspace into *status (EWG_OK,
+ * EWG_ERR_ID_OUT_OF_RANGE or EWG_ERR_INVALID).  Returns EWG_OK or EWG_ERR_CUDA.
+ */
+int ewg_read_status(const void* workspace, void* stream, int* status);
+
+/* Human-readable name of a status code (static storage). */
+const char* ewg_status_string(int status);
+
+/* Detail of the last error returned on the calling thread (static storage, "" if none). */
+const char* ewg_last_error(void);
+
+/* Library ABI version. */
+int ewg_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EWG_H_ */
