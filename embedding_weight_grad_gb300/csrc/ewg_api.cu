@@ -41,7 +41,7 @@ int current_device(int* dev, int* num_sms) {
   if (!d.ready) {
     e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, *dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = ewg::prepare_plan_kernels();
+    e = ewg::prepare_kernels();
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     d.ready = true;
   }
@@ -140,7 +140,7 @@ T* at(void* ws, size_t off) {
 }
 
 int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t H, void* ws,
-            int num_sms, cudaStream_t stream) {
+            cudaStream_t stream) {
   const ewg::Layout L = ewg::make_layout(n, H);
   const ewg::SortPlan sp = ewg::make_sort_plan(V);
   ewg::PlanArgs a{};
@@ -149,22 +149,22 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t H, voi
   a.n = static_cast<int>(n);
   a.num_embeddings = V;
   a.hidden = static_cast<int>(H);
-  a.slices = static_cast<int>(L.slices);
   a.id_bits = sp.id_bits;
   a.passes = sp.passes;
   a.digit_bits = sp.digit_bits;
   a.tiles = static_cast<int>(L.tiles);
   a.header = at<ewg::Header>(ws, L.header);
+  a.tables = at<int>(ws, L.tables);
   a.keys_a = at<uint32_t>(ws, L.keys_a);
   a.vals_a = at<uint32_t>(ws, L.vals_a);
   a.keys_b = at<uint32_t>(ws, L.keys_b);
   a.vals_b = at<uint32_t>(ws, L.vals_b);
   a.chunks = at<int>(ws, L.chunks);
+  a.runs = at<int>(ws, L.runs);
   a.hist = at<uint32_t>(ws, L.hist);
   a.tile_bad = at<int>(ws, L.tile_bad);
-  a.tile_cnt = at<long long>(ws, L.tile_cnt);
-  a.counters = at<int>(ws, L.counters);
-  cudaError_t e = ewg::launch_plan(a, num_sms, stream);
+  a.tile_cnt = at<int4>(ws, L.tile_cnt);
+  cudaError_t e = ewg::launch_plan(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   return EWG_OK;
 }
@@ -181,10 +181,10 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.n = static_cast<int>(n);
   a.hidden = static_cast<int>(H);
   a.num_embeddings = V;
-  a.slices = static_cast<int>(L.slices);
   a.header = at<ewg::Header>(ws, L.header);
+  a.tables = at<int>(ws, L.tables);
   a.chunks = at<int>(ws, L.chunks);
-  a.counters = at<int>(ws, L.counters);
+  a.runs = at<int>(ws, L.runs);
   a.partial = at<float>(ws, L.partial);
   cudaError_t e = ewg::launch_apply(a, grad_dtype == EWG_BF16, mg_dtype == EWG_BF16, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "apply launch");
@@ -225,7 +225,7 @@ int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const voi
   if (rc) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, sms, s);
+  rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, s);
   if (rc) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
                   num_embeddings, hidden, main_grad_row_stride, workspace, sms, s);
@@ -240,7 +240,7 @@ int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_emb
   if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
   if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
-  return do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, sms,
+  return do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace,
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -285,6 +285,7 @@ const char* ewg_status_string(int status) {
     case EWG_ERR_INVALID: return "EWG_ERR_INVALID";
     case EWG_ERR_CUDA: return "EWG_ERR_CUDA";
     case EWG_ERR_ID_OUT_OF_RANGE: return "EWG_ERR_ID_OUT_OF_RANGE";
+    case EWG_ERR_TIMEOUT: return "EWG_ERR_TIMEOUT";
     default: return "EWG_ERR_UNKNOWN";
   }
 }

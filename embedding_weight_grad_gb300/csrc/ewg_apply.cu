@@ -1,28 +1,58 @@
-// Apply kernel: chunk partial sums, ordered long-run combine, add into main_grad.
+// Apply kernels: chunk partial sums, ordered long-run combine, add into main_grad.
 //
 // Counterpart of _partial_sums_kernel and _long_run_sums_kernel (Megatron Core API
-// docs, core.fusions.fused_embedding_wgrad, "Functions"), fused into one persistent
-// kernel.  The arithmetic is the module docstring's: per chunk of at most NROWS rows,
-// part = ((0 + g_0) + g_1) + ... in fp32 and position order; per token,
-// t = ((0 + part_0) + part_1) + ... in chunk order; w = round_to_grad_dtype(t);
-// main_grad[id] = round_to_main_grad_dtype(main_grad[id] + w) in fp32.
+// docs, core.fusions.fused_embedding_wgrad, "Functions").  The arithmetic is the
+// module docstring's: per chunk of at most NROWS rows, part = ((0 + g_0) + g_1) + ...
+// in fp32 and position order; per token, t = ((0 + part_0) + part_1) + ... in chunk
+// order; w = round_to_grad_dtype(t); main_grad[id] = round_to_main_grad_dtype(
+// main_grad[id] + w) computed in fp32.
 //
-// Work item = (chunk, 256-column slice), one warp each; lane l owns 8 consecutive
-// columns, so every gathered grad row is read as one 16-byte load per lane (bf16)
-// and a warp covers 512 contiguous bytes of it.  All rows of a chunk are loaded
-// before the first add.  A token with a single chunk is finished by the warp that
-// summed it.  For a longer token each warp stores its fp32 partial row, and the
-// last warp to arrive at the (token, slice) counter adds all of the token's
-// partials in chunk order; which warp that is does not change any value.
+// Two persistent kernels, each a bulk-copy pipeline:
+//   apply_long   every (chunk of a long run, 1024-column tile): part -> fp32 partial row
+//   apply_rest   every (long run, 512-column group): fold the run's partial rows in
+//                chunk order, round, add into main_grad; then every (short run's
+//                chunk, 1024-column tile): part, round, add into main_grad
+// The kernel boundary orders every partial row before its fold, so no CTA waits for
+// another.  Within a CTA one producer thread issues cp.async.bulk copies of the
+// gathered grad row segments (or partial rows) and of the main_grad segment into a
+// 96 KB shared-memory ring, completing on a per-slot mbarrier; four consumer warps
+// (8 columns per thread) take the slots in order, add the rows in order from shared
+// memory and release the slot.  The depth of the ring, not the register file, sets
+// how many bytes each SM keeps in flight.
 #include <cuda_bf16.h>
 
 #include "ewg.h"
 #include "ewg_internal.cuh"
+#include "ewg_ptx.cuh"
 
 namespace ewg {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr uint32_t kSpinLimit = 1u << 22;   // bounded mbarrier waits
+
+enum ItemKind { kEnd = -1, kShortChunk = 0, kLongChunk = 1, kCombine = 2 };
+
+struct Item {
+  int off;        // byte offset of the item in the ring
+  int rows;       // grad rows (chunks) or partial rows (combine) in the ring
+  int id;         // main_grad row
+  int prow;       // partial row to write (long chunk)
+  int col0;       // first column
+  int cols;       // columns
+  int kind;
+  int flags;      // combine: bit 0 first batch, bit 1 last batch
+};
+
+struct Smem {
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  Item info[kSlots];
+  int prefix[3][kMaxParts + 1];   // long chunks, short chunks, long runs
+  int offset[3][kMaxParts];
+  int num_parts;
+  int abort;
+};
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
@@ -33,93 +63,67 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return l | (h << 16);
 }
 
-__device__ __forceinline__ uint4 load_stream_u4(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
+// Waits for the phase of `bar` with the given parity; false if the wait gave up
+// (limit reached or another thread of the CTA aborted).
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort) return false;
+  }
+  return false;
 }
 
-// fp32 partial sum of one chunk's rows over this lane's 8 columns.  `word` holds
-// descriptor word `lane`; words 0..9 are the chunk's token positions.
-template <bool GBF16>
-__device__ __forceinline__ void chunk_partial(const ApplyArgs& a, int word, int len, int col,
-                                              bool active, float part[8]) {
-#pragma unroll
-  for (int e = 0; e < 8; ++e) part[e] = 0.0f;
-  if constexpr (GBF16) {
-    const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(a.grad) + col;
-    uint4 v[kNrows];
-#pragma unroll
-    for (int k = 0; k < kNrows; ++k) {
-      const int p = __shfl_sync(kFull, word, kDescPos + k);
-      v[k] = make_uint4(0, 0, 0, 0);
-      if (k < len && active) v[k] = load_stream_u4(g + static_cast<long long>(p) * a.grad_stride);
-    }
-#pragma unroll
-    for (int k = 0; k < kNrows; ++k) {
-      if (k < len) {
-        part[0] = part[0] + bf16_lo(v[k].x);
-        part[1] = part[1] + bf16_hi(v[k].x);
-        part[2] = part[2] + bf16_lo(v[k].y);
-        part[3] = part[3] + bf16_hi(v[k].y);
-        part[4] = part[4] + bf16_lo(v[k].z);
-        part[5] = part[5] + bf16_hi(v[k].z);
-        part[6] = part[6] + bf16_lo(v[k].w);
-        part[7] = part[7] + bf16_hi(v[k].w);
-      }
-    }
+__device__ void give_up(const ApplyArgs& a, volatile int* abort) {
+  *abort = 1;
+  atomicExch(const_cast<int*>(&a.header->status), kStatusTimeout);
+}
+
+// Adds 8 elements of a row held in shared memory, in order, into acc.
+template <bool BF16>
+__device__ __forceinline__ void add_row(float acc[8], const unsigned char* p) {
+  if constexpr (BF16) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    acc[0] = acc[0] + bf16_lo(v.x);
+    acc[1] = acc[1] + bf16_hi(v.x);
+    acc[2] = acc[2] + bf16_lo(v.y);
+    acc[3] = acc[3] + bf16_hi(v.y);
+    acc[4] = acc[4] + bf16_lo(v.z);
+    acc[5] = acc[5] + bf16_hi(v.z);
+    acc[6] = acc[6] + bf16_lo(v.w);
+    acc[7] = acc[7] + bf16_hi(v.w);
   } else {
-    const float* g = static_cast<const float*>(a.grad) + col;
-    uint4 v[kNrows][2];
-#pragma unroll
-    for (int k = 0; k < kNrows; ++k) {
-      const int p = __shfl_sync(kFull, word, kDescPos + k);
-      v[k][0] = v[k][1] = make_uint4(0, 0, 0, 0);
-      if (k < len && active) {
-        const float* r = g + static_cast<long long>(p) * a.grad_stride;
-        v[k][0] = load_stream_u4(r);
-        v[k][1] = load_stream_u4(r + 4);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kNrows; ++k) {
-      if (k < len) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          part[4 * h + 0] = part[4 * h + 0] + __uint_as_float(v[k][h].x);
-          part[4 * h + 1] = part[4 * h + 1] + __uint_as_float(v[k][h].y);
-          part[4 * h + 2] = part[4 * h + 2] + __uint_as_float(v[k][h].z);
-          part[4 * h + 3] = part[4 * h + 3] + __uint_as_float(v[k][h].w);
-        }
-      }
-    }
+    const float4 x = *reinterpret_cast<const float4*>(p);
+    const float4 y = *reinterpret_cast<const float4*>(p + 16);
+    acc[0] = acc[0] + x.x;
+    acc[1] = acc[1] + x.y;
+    acc[2] = acc[2] + x.z;
+    acc[3] = acc[3] + x.w;
+    acc[4] = acc[4] + y.x;
+    acc[5] = acc[5] + y.y;
+    acc[6] = acc[6] + y.z;
+    acc[7] = acc[7] + y.w;
   }
 }
 
-// w = round_g(t); main_grad[id][col..col+8) = round_mg(main_grad + w) in fp32.
+// w = round_g(t); out = round_mg(m + w) in fp32, m from the ring; stored to main_grad.
 template <bool GBF16, bool MBF16>
-__device__ __forceinline__ void finish(const ApplyArgs& a, int id, int col, const float t[8]) {
+__device__ __forceinline__ void finish(const ApplyArgs& a, const float t[8],
+                                       const unsigned char* m_smem, int id, int col) {
   float w[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    w[e] = GBF16 ? __bfloat162float(__float2bfloat16_rn(t[e])) : t[e];
-  }
+  for (int e = 0; e < 8; ++e) w[e] = GBF16 ? __bfloat162float(__float2bfloat16_rn(t[e])) : t[e];
   if constexpr (MBF16) {
-    uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.main_grad) +
-                                        static_cast<long long>(id) * a.mg_stride + col);
-    const uint4 m = *p;
+    const uint4 m = *reinterpret_cast<const uint4*>(m_smem);
     uint4 o;
     o.x = pack_bf16(bf16_lo(m.x) + w[0], bf16_hi(m.x) + w[1]);
     o.y = pack_bf16(bf16_lo(m.y) + w[2], bf16_hi(m.y) + w[3]);
     o.z = pack_bf16(bf16_lo(m.z) + w[4], bf16_hi(m.z) + w[5]);
     o.w = pack_bf16(bf16_lo(m.w) + w[6], bf16_hi(m.w) + w[7]);
-    *p = o;
+    *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.main_grad) +
+                              static_cast<long long>(id) * a.mg_stride + col) = o;
   } else {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(a.main_grad) +
-                                          static_cast<long long>(id) * a.mg_stride + col);
-    float4 m0 = p[0], m1 = p[1];
+    float4 m0 = *reinterpret_cast<const float4*>(m_smem);
+    float4 m1 = *reinterpret_cast<const float4*>(m_smem + 16);
     m0.x = m0.x + w[0];
     m0.y = m0.y + w[1];
     m0.z = m0.z + w[2];
@@ -128,98 +132,382 @@ __device__ __forceinline__ void finish(const ApplyArgs& a, int id, int col, cons
     m1.y = m1.y + w[5];
     m1.z = m1.z + w[6];
     m1.w = m1.w + w[7];
-    p[0] = m0;
-    p[1] = m1;
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(a.main_grad) +
+                                            static_cast<long long>(id) * a.mg_stride + col);
+    dst[0] = m0;
+    dst[1] = m1;
   }
+}
+
+// Index of list element `ord` (ordinals increase along the calls) given the
+// per-partition prefix counts and offsets; `cur` is the partition cursor.
+__device__ __forceinline__ int list_index(const int* prefix, const int* offset, int parts, int ord,
+                                          int& cur) {
+  while (cur + 1 < parts && ord >= prefix[cur + 1]) ++cur;
+  return offset[cur] + (ord - prefix[cur]);
+}
+
+struct Desc {
+  int4 w[4];
+};
+
+__device__ __forceinline__ Desc load_desc(const int* chunks, int di) {
+  const int4* p = reinterpret_cast<const int4*>(chunks + static_cast<long long>(di) * kChunkWords);
+  Desc d;
+  d.w[0] = __ldg(p);
+  d.w[1] = __ldg(p + 1);
+  d.w[2] = __ldg(p + 2);
+  d.w[3] = __ldg(p + 3);
+  return d;
+}
+
+__device__ __forceinline__ int desc_pos(const Desc& d, int k) {
+  const int4& v = d.w[k >> 2];
+  switch (k & 3) {
+    case 0: return v.x;
+    case 1: return v.y;
+    case 2: return v.z;
+    default: return v.w;
+  }
+}
+
+// The single producer thread of a CTA.
+template <bool GBF16, bool MBF16, bool LONG>
+struct Producer {
+  const ApplyArgs& a;
+  Smem& s;
+  unsigned char* ring;
+  int q = 0;            // items issued
+  int rel = 0;          // items known to be consumed
+  uint32_t head = 0, tail = 0;
+  uint64_t pol_stream;
+  bool ok = true;
+
+  __device__ Producer(const ApplyArgs& args, Smem& sm, unsigned char* r)
+      : a(args), s(sm), ring(r), pol_stream(ptx::policy_evict_first()) {}
+
+  __device__ bool confirm_oldest() {
+    const int slot = rel % kSlots;
+    if (!wait_phase(&s.empty[slot], (rel / kSlots) & 1, &s.abort)) return false;
+    ++rel;
+    head = rel < q ? static_cast<uint32_t>(s.info[rel % kSlots].off) : tail;
+    return true;
+  }
+
+  // Offset of `bytes` free, contiguous ring bytes (items leave in issue order).
+  __device__ int reserve(uint32_t bytes) {
+    while (q - rel >= kSlots)
+      if (!confirm_oldest()) return -1;
+    for (;;) {
+      if (q == rel) head = tail = 0;
+      const bool full = q > rel && head == tail;
+      if (!full) {
+        if (head <= tail) {
+          if (tail + bytes <= static_cast<uint32_t>(kRingBytes)) return static_cast<int>(tail);
+          if (bytes <= head) return 0;
+        } else if (tail + bytes <= head) {
+          return static_cast<int>(tail);
+        }
+      }
+      if (!confirm_oldest()) return -1;
+    }
+  }
+
+  // Publishes item info and arms the slot's barrier for `bytes` of copies.
+  __device__ uint64_t* open(const Item& it, uint32_t bytes) {
+    const int slot = q % kSlots;
+    s.info[slot] = it;
+    tail = static_cast<uint32_t>(it.off) + bytes;
+    ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive_expect_tx(&s.full[slot], bytes);
+    ++q;
+    return &s.full[slot];
+  }
+
+  __device__ void copy(int dst_off, const void* src, uint32_t bytes, uint64_t* bar) {
+    ptx::bulk_g2s(ring + dst_off, src, bytes, bar, pol_stream);
+  }
+
+  // One (chunk, column tile) item: the chunk's grad row segments, plus the main_grad
+  // segment when the run has no other chunk.
+  __device__ bool chunk_item(const Desc& d, int tile) {
+    const int col0 = tile * kColTile;
+    const int cols = min(kColTile, a.hidden - col0);
+    const int meta = d.w[2].w;
+    const int len = meta & 15;
+    const int id = d.w[2].z;
+    const uint32_t row_bytes = cols * (GBF16 ? 2 : 4);
+    const uint32_t mg_bytes = LONG ? 0u : cols * (MBF16 ? 2 : 4);
+    const uint32_t bytes = len * row_bytes + mg_bytes;
+    const int off = reserve(bytes);
+    if (off < 0) return false;
+    Item it{off, len, id, d.w[3].x, col0, cols, LONG ? kLongChunk : kShortChunk, 0};
+    uint64_t* bar = open(it, bytes);
+    const char* g = static_cast<const char*>(a.grad);
+    const long long gsz = GBF16 ? 2 : 4;
+#pragma unroll
+    for (int k = 0; k < kNrows; ++k) {
+      if (k < len) {
+        const long long p = desc_pos(d, k);
+        copy(off + k * row_bytes, g + (p * a.grad_stride + col0) * gsz, row_bytes, bar);
+      }
+    }
+    if (!LONG) {
+      const char* m = static_cast<const char*>(a.main_grad);
+      const long long msz = MBF16 ? 2 : 4;
+      copy(off + len * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
+           mg_bytes, bar);
+    }
+    return true;
+  }
+
+  // One (long run, 512-column group) fold, as batches of partial rows; the last batch
+  // also brings the main_grad segment.
+  __device__ bool combine_task(int4 run, int group) {
+    const int prow0 = run.x, C = run.y, id = run.z;
+    const int col0 = group * kCombineCols;
+    const int cols = min(kCombineCols, a.hidden - col0);
+    const uint32_t row_bytes = cols * 4;
+    const uint32_t mg_bytes = cols * (MBF16 ? 2 : 4);
+    for (int b0 = 0; b0 < C; b0 += kCombineBatch) {
+      const int nb = min(kCombineBatch, C - b0);
+      const bool last = b0 + nb == C;
+      const uint32_t bytes = nb * row_bytes + (last ? mg_bytes : 0u);
+      const int off = reserve(bytes);
+      if (off < 0) return false;
+      Item it{off, nb, id, -1, col0, cols, kCombine, (b0 == 0 ? 1 : 0) | (last ? 2 : 0)};
+      uint64_t* bar = open(it, bytes);
+      for (int k = 0; k < nb; ++k) {
+        const float* src = a.partial + static_cast<long long>(prow0 + b0 + k) * a.hidden + col0;
+        copy(off + k * row_bytes, src, row_bytes, bar);
+      }
+      if (last) {
+        const char* m = static_cast<const char*>(a.main_grad);
+        const long long msz = MBF16 ? 2 : 4;
+        copy(off + nb * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
+             mg_bytes, bar);
+      }
+    }
+    return true;
+  }
+
+  __device__ void finish_stream() {
+    if (ok) {
+      while (q - rel >= kSlots)
+        if (!confirm_oldest()) {
+          ok = false;
+          break;
+        }
+    }
+    if (ok) {
+      const int slot = q % kSlots;
+      s.info[slot].kind = kEnd;
+      ptx::mbar_arrive(&s.full[slot]);
+      ++q;
+      return;
+    }
+    // gave up: let the copies already in flight land before the CTA exits
+    for (int r = rel; r < q; ++r) {
+      uint64_t* bar = &s.full[r % kSlots];
+      for (uint32_t i = 0; i < kSpinLimit && !ptx::mbar_try_wait(bar, (r / kSlots) & 1); ++i) {
+      }
+    }
+  }
+};
+
+template <bool GBF16, bool MBF16, bool LONG>
+__device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
+  Producer<GBF16, MBF16, LONG> P(a, s, ring);
+  const int parts = s.num_parts;
+  const int T = static_cast<int>((a.hidden + kColTile - 1) / kColTile);
+  const long long G = gridDim.x;
+  long long idx = blockIdx.x;
+
+  if (!LONG) {   // combine tasks first
+    const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
+    const long long n_tasks = static_cast<long long>(s.prefix[2][parts]) * Tc;
+    int cur = 0;
+    for (; idx < n_tasks && P.ok; idx += G) {
+      const int r = static_cast<int>(idx / Tc);
+      const int group = static_cast<int>(idx - static_cast<long long>(r) * Tc);
+      const int ri = list_index(s.prefix[2], s.offset[2], parts, r, cur);
+      const int4 run = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
+      P.ok = P.combine_task(run, group);
+    }
+    idx -= n_tasks;   // now an ordinal into the chunk items
+  }
+
+  const int list = LONG ? 0 : 1;
+  const long long n_items = static_cast<long long>(s.prefix[list][parts]) * T;
+  int cur = 0;
+  // two descriptors in flight ahead of the item being issued
+  long long o0 = idx, o1 = idx + G;
+  Desc d0{}, d1{};
+  if (o0 < n_items) d0 = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
+                                                        static_cast<int>(o0 / T), cur));
+  if (o1 < n_items) d1 = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
+                                                        static_cast<int>(o1 / T), cur));
+  while (o0 < n_items && P.ok) {
+    const long long o2 = o1 + G;
+    Desc d2{};
+    if (o2 < n_items) d2 = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
+                                                          static_cast<int>(o2 / T), cur));
+    P.ok = P.chunk_item(d0, static_cast<int>(o0 % T));
+    o0 = o1;
+    d0 = d1;
+    o1 = o2;
+    d1 = d2;
+  }
+  P.finish_stream();
 }
 
 template <bool GBF16, bool MBF16>
-__global__ void __launch_bounds__(kApplyThreads) apply_kernel(ApplyArgs a) {
-  Header* hdr = const_cast<Header*>(a.header);
-  if (hdr->status != EWG_OK) return;
-  if (hdr->n != a.n || hdr->hidden != a.hidden || hdr->num_embeddings != a.num_embeddings) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) hdr->status = EWG_ERR_INVALID;
-    return;
-  }
-  const int S = a.slices;
-  const long long items = static_cast<long long>(hdr->num_chunks) * S;
-  const int lane = threadIdx.x & 31;
-  constexpr int kWarps = kApplyThreads / 32;
-  const long long first = static_cast<long long>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const long long stride = static_cast<long long>(gridDim.x) * kWarps;
-
-  for (long long it = first; it < items; it += stride) {
-    const int ci = static_cast<int>(it / S);
-    const int j = static_cast<int>(it - static_cast<long long>(ci) * S);
-    const int word = lane < kChunkWords ? a.chunks[static_cast<long long>(ci) * kChunkWords + lane] : 0;
-    const int id = __shfl_sync(kFull, word, kDescId);
-    const int meta = __shfl_sync(kFull, word, kDescMeta);
-    const int lc = __shfl_sync(kFull, word, kDescLong);
-    const int C = __shfl_sync(kFull, word, kDescNumChunks);
-    const int len = meta & 15, c = meta >> 4;
-    const int col = j * kSliceCols + lane * 8;
-    const bool active = col < a.hidden;
-
-    float part[8];
-    chunk_partial<GBF16>(a, word, len, col, active, part);
-
-    if (lc < 0) {  // the token's only chunk: t = 0 + part
-      float t[8];
+__device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) {
+  const int t = threadIdx.x, lane = t & 31;
+  float total[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) t[e] = 0.0f + part[e];
-      if (active) finish<GBF16, MBF16>(a, id, col, t);
-      continue;
+  for (int e = 0; e < 8; ++e) total[e] = 0.0f;
+  for (int q = 0;; ++q) {
+    const int slot = q % kSlots;
+    if (!wait_phase(&s.full[slot], (q / kSlots) & 1, &s.abort)) {
+      give_up(a, &s.abort);
+      return;
     }
-
-    const long long lc0 = lc - c;  // partial row of the token's first chunk
-    if (active) {
-      float4* dst = reinterpret_cast<float4*>(a.partial + static_cast<long long>(lc) * a.hidden + col);
-      dst[0] = make_float4(part[0], part[1], part[2], part[3]);
-      dst[1] = make_float4(part[4], part[5], part[6], part[7]);
-    }
-    __threadfence();
-    __syncwarp();
-    int prior = 0;
-    if (lane == 0) prior = atomicAdd(a.counters + lc0 * S + j, 1);
-    prior = __shfl_sync(kFull, prior, 0);
-    if (prior != C - 1) continue;  // another warp will arrive later and combine
-
-    __threadfence();
-    if (active) {
-      const float* src = a.partial + lc0 * a.hidden + col;
-      float t[8];
+    const Item it = s.info[slot];
+    if (it.kind == kEnd) return;
+    const int c = t * 8;
+    if (c < it.cols) {
+      const unsigned char* base = ring + it.off;
+      if (it.kind == kCombine) {
+        const uint32_t row_bytes = it.cols * 4;
+        if (it.flags & 1) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) t[e] = 0.0f;
-#pragma unroll 4
-      for (int q = 0; q < C; ++q) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(src + static_cast<long long>(q) * a.hidden));
-        const float4 y = __ldcg(reinterpret_cast<const float4*>(src + static_cast<long long>(q) * a.hidden + 4));
-        t[0] = t[0] + x.x;
-        t[1] = t[1] + x.y;
-        t[2] = t[2] + x.z;
-        t[3] = t[3] + x.w;
-        t[4] = t[4] + y.x;
-        t[5] = t[5] + y.y;
-        t[6] = t[6] + y.z;
-        t[7] = t[7] + y.w;
+          for (int e = 0; e < 8; ++e) total[e] = 0.0f;   // "in order starting from 0"
+        }
+        for (int k = 0; k < it.rows; ++k) add_row<false>(total, base + k * row_bytes + c * 4);
+        if (it.flags & 2)
+          finish<GBF16, MBF16>(a, total, base + it.rows * row_bytes + c * (MBF16 ? 2 : 4), it.id,
+                               it.col0 + c);
+      } else {
+        const uint32_t row_bytes = it.cols * (GBF16 ? 2 : 4);
+        float part[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[e] = 0.0f;
+        for (int k = 0; k < it.rows; ++k)
+          add_row<GBF16>(part, base + k * row_bytes + c * (GBF16 ? 2 : 4));
+        if (it.kind == kLongChunk) {
+          float4* dst = reinterpret_cast<float4*>(a.partial + static_cast<long long>(it.prow) * a.hidden +
+                                                  it.col0 + c);
+          dst[0] = make_float4(part[0], part[1], part[2], part[3]);
+          dst[1] = make_float4(part[4], part[5], part[6], part[7]);
+        } else {   // the run's only chunk: t = 0 + part
+          float tt[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) tt[e] = 0.0f + part[e];
+          finish<GBF16, MBF16>(a, tt, base + it.rows * row_bytes + c * (MBF16 ? 2 : 4), it.id,
+                               it.col0 + c);
+        }
       }
-      finish<GBF16, MBF16>(a, id, col, t);
     }
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&s.empty[slot]);
   }
 }
 
-template <bool G, bool M>
-cudaError_t launch_variant(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
-  static int blocks_per_sm = 0;  // the same for every device of one architecture
+template <bool GBF16, bool MBF16, bool LONG>
+__global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw;
+  Smem& s = *reinterpret_cast<Smem*>(smem_raw + kRingBytes);
+  const int t = threadIdx.x;
+  if (t == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      ptx::mbar_init(&s.full[i], 1);
+      ptx::mbar_init(&s.empty[i], kConsumerWarps);
+    }
+    ptx::fence_mbar_init();
+    s.abort = 0;
+  }
+  // every CTA waits for the previous kernel, so this grid never completes before it
+  ptx::pdl_wait_prior_grid();
+  if (LONG) ptx::pdl_launch_dependents();
+
+  const Header* h = a.header;
+  if (t == 0) {   // one reader decides for the whole CTA
+    int go = h->status == EWG_OK;
+    if (go && (h->n != a.n || h->hidden != a.hidden || h->num_embeddings != a.num_embeddings)) {
+      if (blockIdx.x == 0) const_cast<Header*>(h)->status = kStatusInvalid;
+      go = 0;
+    }
+    s.num_parts = go ? h->num_parts : -1;
+  }
+  __syncthreads();
+  if (s.num_parts < 0) return;
+  if (t < 32) {   // partition tables -> per-list prefix counts
+    const int parts = s.num_parts;
+    for (int list = 0; list < 3; ++list) {
+      const int cnt_tab = list == 0 ? kLongCnt : list == 1 ? kShortCnt : kRunCnt;
+      const int off_tab = list == 0 ? kLongOff : list == 1 ? kShortOff : kRunOff;
+      int carry = 0;
+      for (int p0 = 0; p0 < parts; p0 += 32) {
+        const int p = p0 + t;
+        const int c = p < parts ? a.tables[cnt_tab * kMaxParts + p] : 0;
+        if (p < parts) s.offset[list][p] = a.tables[off_tab * kMaxParts + p];
+        int x = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(kFull, x, o);
+          if (t >= o) x += y;
+        }
+        if (p < parts) s.prefix[list][p] = carry + x - c;
+        carry += __shfl_sync(kFull, x, 31);
+      }
+      if (t == 0) s.prefix[list][parts] = carry;
+    }
+  }
+  __syncthreads();
+
+  if (t >= kConsumers) {
+    if (t == kConsumers) produce<GBF16, MBF16, LONG>(a, s, ring);
+    return;
+  }
+  consume<GBF16, MBF16>(a, s, ring);
+}
+
+constexpr size_t kApplySmem = kRingBytes + sizeof(Smem);
+
+template <bool G, bool M, bool LONG>
+cudaError_t launch_one(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
+  static int blocks_per_sm = 0;
   if (blocks_per_sm == 0) {
+    cudaError_t e = cudaFuncSetAttribute(apply_kernel<G, M, LONG>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kApplySmem));
+    if (e != cudaSuccess) return e;
     int b = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, apply_kernel<G, M>,
-                                                                  kApplyThreads, 0);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, apply_kernel<G, M, LONG>, kApplyThreads,
+                                                      kApplySmem);
     if (e != cudaSuccess) return e;
     blocks_per_sm = b > 0 ? b : 1;
   }
-  apply_kernel<G, M><<<num_sms * blocks_per_sm, kApplyThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms * blocks_per_sm);
+  cfg.blockDim = dim3(kApplyThreads);
+  cfg.dynamicSmemBytes = kApplySmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, apply_kernel<G, M, LONG>, a);
+}
+
+template <bool G, bool M>
+cudaError_t launch_pair(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
+  cudaError_t e = launch_one<G, M, true>(a, num_sms, stream);
+  if (e != cudaSuccess) return e;
+  return launch_one<G, M, false>(a, num_sms, stream);
 }
 
 }  // namespace
@@ -227,11 +515,11 @@ cudaError_t launch_variant(const ApplyArgs& a, int num_sms, cudaStream_t stream)
 cudaError_t launch_apply(const ApplyArgs& a, int grad_bf16, int mg_bf16, int num_sms,
                          cudaStream_t stream) {
   if (grad_bf16) {
-    return mg_bf16 ? launch_variant<true, true>(a, num_sms, stream)
-                   : launch_variant<true, false>(a, num_sms, stream);
+    return mg_bf16 ? launch_pair<true, true>(a, num_sms, stream)
+                   : launch_pair<true, false>(a, num_sms, stream);
   }
-  return mg_bf16 ? launch_variant<false, true>(a, num_sms, stream)
-                 : launch_variant<false, false>(a, num_sms, stream);
+  return mg_bf16 ? launch_pair<false, true>(a, num_sms, stream)
+                 : launch_pair<false, false>(a, num_sms, stream);
 }
 
 }  // namespace ewg

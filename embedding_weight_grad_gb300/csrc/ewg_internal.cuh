@@ -1,18 +1,21 @@
 // Internal declarations shared by the library's translation units.
 //
-// Data layout in the caller's workspace (each region 256-byte aligned):
+// Vocabulary.  A "run" is the set of sorted slots of one token id; its slots hold the
+// token's positions in ascending order.  A "chunk" is up to NROWS consecutive slots of
+// a run, counted from the run's first slot.  A run is "long" when it has more than
+// NROWS slots (more than one chunk).
 //
-//   Header        status words, chunk counts and the stamp of the plan
-//   keys/vals x2  ping-pong buffers of the radix sort: id (u32) and position (u32)
-//   chunks        one 64-byte descriptor per chunk: up to 10 token positions, the id,
-//                 chunk index c within its run, chunks in the run C, and the index
-//                 of its fp32 partial row when the run is long
-//   tile scratch  per-tile digit histograms, bad-id counts and listing counts
-//   counters      one arrival counter per (long-run chunk, 256-column slice)
-//   partial       fp32 [max long-run chunks][hidden] chunk partial sums
+// Work lists the plan leaves in the caller's workspace, grouped in partitions (one
+// partition on the multi-tile path, one per hash partition of the ids otherwise):
+//   long chunks   descriptors of every chunk of every long run
+//   short chunks  descriptors of the single chunk of every other run
+//   long runs     (first partial row, number of chunks C, id) per long run
+// A partition's lists are contiguous; per-partition counts and offsets sit in the
+// partition tables.  The apply kernels walk the lists partition by partition.
 //
-// A "chunk" is up to NROWS consecutive sorted slots of one token's run, counted from
-// the run's first slot; a run is "long" when it has more than NROWS slots.
+// Workspace layout (each region 256-byte aligned):
+//   Header | tables | keys/vals x2 (multi-tile sort) | chunk descriptors | run table |
+//   tile scratch (histograms, bad-id counts, listing counts) | fp32 partial rows
 #pragma once
 
 #include <cstddef>
@@ -23,60 +26,76 @@
 namespace ewg {
 
 constexpr int kNrows = 10;           // chunk length: NROWS_PER_THREAD of PyTorch's backward
-constexpr int kSliceCols = 256;      // columns one warp covers (32 lanes x 8 elements)
-constexpr int kChunkWords = 16;      // 64-byte chunk descriptor
-constexpr int kDescPos = 0;          // words 0..9: token positions, in position order
-constexpr int kDescId = 10;          // word 10: the token id (main_grad row)
-constexpr int kDescMeta = 11;        // word 11: len | (c << 4)
-constexpr int kDescLong = 12;        // word 12: partial row of this chunk, -1 for short runs
-constexpr int kDescNumChunks = 13;   // word 13: C, the number of chunks of the run
 
-// Single-CTA plan (sort + listing entirely in shared memory).
-constexpr int kSmallThreads = 1024;
-constexpr int kSmallItems = 8;
-constexpr int kSmallMaxN = kSmallThreads * kSmallItems;   // 8192 tokens
+// Chunk descriptor: 16 x int32 = 64 bytes.
+constexpr int kChunkWords = 16;
+constexpr int kDescPos = 0;          // words 0..9: token positions, in position order
+constexpr int kDescId = 10;          // token id (main_grad row)
+constexpr int kDescMeta = 11;        // len | (c << 4), c = chunk index within the run
+constexpr int kDescPartial = 12;     // partial row of this chunk (long runs), else -1
+constexpr int kDescNumChunks = 13;   // C, chunks of the run
+
+// Long-run table entry: 4 x int32.
+constexpr int kRunWords = 4;         // first partial row, C, id, unused
+
+// Partition tables: kTables arrays of kMaxParts ints.
+constexpr int kMaxParts = 128;
+enum Table { kLongCnt = 0, kLongOff, kShortCnt, kShortOff, kRunCnt, kRunOff, kTables };
+
+// Hashed plan (up to 8192 tokens): one CTA per hash partition of the ids.
+constexpr int kHashParts = 64;
+constexpr int kHashThreads = 512;
+constexpr int kHashItems = 16;
+constexpr int kHashMaxN = kHashThreads * kHashItems;      // 8192 tokens
 constexpr int kMaxDigitBits = 9;                          // 512 buckets per radix pass
 
-// Multi-CTA plan.
+// Multi-tile plan.
 constexpr int kTileThreads = 256;
 constexpr int kTileItems = 8;
 constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
 
-// Apply kernel.
-constexpr int kApplyThreads = 256;
+// Apply kernels.
+constexpr int kColTile = 1024;        // columns of one chunk item (128 consumers x 8)
+constexpr int kCombineCols = 512;     // columns of one combine task
+constexpr int kCombineBatch = 8;      // partial rows per combine ring item
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kApplyThreads = kConsumers + 32;            // + one producer warp
+constexpr int kRingBytes = 96 * 1024;
+constexpr int kSlots = 16;
+
+enum DeviceStatus { kStatusOk = 0, kStatusInvalid = 2, kStatusBadId = 4, kStatusTimeout = 5 };
 
 struct Header {
   int status;            // EWG_OK or the device-detected error of the last call
-  int num_chunks;
-  int num_long_chunks;
-  int bad_ids;
   int n;                 // stamp of the plan: tokens, hidden, num_embeddings
   int hidden;
+  int num_parts;
   long long num_embeddings;
-  int pad[56];
+  int bad_ids;
+  int pad[57];
 };
 static_assert(sizeof(Header) == 256, "header is one 256-byte region");
 
-struct Layout {
-  size_t header, keys_a, vals_a, keys_b, vals_b, chunks, hist, tile_bad, tile_cnt, counters,
-      partial, total;
-  int64_t n, hidden, tiles, slices, max_long_chunks;
-};
-
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+// Long runs of L >= 11 rows have ceil(L/10) <= 2L/11 chunks; partition b of the hashed
+// plan starts its partial rows at floor(2 S_b / 11) + b (S_b: tokens of partitions < b).
+inline int64_t max_partial_rows(int64_t n) { return 2 * n / 11 + kMaxParts + 1; }
+inline int64_t max_long_runs(int64_t n) { return n / 11 + kMaxParts + 1; }
 
-// Every long run of L >= 11 rows has ceil(L/10) <= 2L/11 chunks.
-inline int64_t max_long_chunks(int64_t n) { return 2 * n / 11 + 1; }
+struct Layout {
+  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, hist, tile_bad, tile_cnt,
+      partial, total;
+  int64_t n, hidden, tiles;
+};
 
 inline Layout make_layout(int64_t n, int64_t hidden) {
   Layout L{};
   L.n = n;
   L.hidden = hidden;
   L.tiles = ceil_div(n, kTile);
-  L.slices = ceil_div(hidden, kSliceCols);
-  L.max_long_chunks = max_long_chunks(n);
   const int64_t n_pad = L.tiles * kTile;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -85,16 +104,17 @@ inline Layout make_layout(int64_t n, int64_t hidden) {
     return at;
   };
   L.header = take(sizeof(Header));
+  L.tables = take(sizeof(int) * kTables * kMaxParts);
   L.keys_a = take(n_pad * 4);
   L.vals_a = take(n_pad * 4);
   L.keys_b = take(n_pad * 4);
   L.vals_b = take(n_pad * 4);
   L.chunks = take(static_cast<size_t>(n) * kChunkWords * 4);
+  L.runs = take(static_cast<size_t>(max_long_runs(n)) * kRunWords * 4);
   L.hist = take(static_cast<size_t>(L.tiles) * (1 << kMaxDigitBits) * 4);
   L.tile_bad = take(static_cast<size_t>(L.tiles) * 4);
-  L.tile_cnt = take(static_cast<size_t>(L.tiles) * 8);
-  L.counters = take(static_cast<size_t>(L.max_long_chunks) * L.slices * 4);
-  L.partial = take(static_cast<size_t>(L.max_long_chunks) * hidden * 4);
+  L.tile_cnt = take(static_cast<size_t>(L.tiles) * 16);
+  L.partial = take(static_cast<size_t>(max_partial_rows(n)) * hidden * 4);
   L.total = off;
   return L;
 }
@@ -124,29 +144,27 @@ inline SortPlan make_sort_plan(int64_t num_embeddings) {
   return s;
 }
 
-// Arguments of the plan kernels.
 struct PlanArgs {
   const void* ids;
   int ids_int64;
   int n;
   long long num_embeddings;
   int hidden;
-  int slices;
   int id_bits, passes, digit_bits;
   int tiles;
   Header* header;
+  int* tables;           // [kTables][kMaxParts]
   uint32_t* keys_a;
   uint32_t* vals_a;
   uint32_t* keys_b;
   uint32_t* vals_b;
   int* chunks;
+  int* runs;
   uint32_t* hist;
   int* tile_bad;
-  long long* tile_cnt;
-  int* counters;
+  int4* tile_cnt;        // per tile: long chunks, short chunks, long runs
 };
 
-// Arguments of the apply kernel.
 struct ApplyArgs {
   const void* grad;
   long long grad_stride;   // elements
@@ -155,16 +173,18 @@ struct ApplyArgs {
   int n;
   int hidden;
   long long num_embeddings;
-  int slices;
   const Header* header;
+  const int* tables;
   const int* chunks;
-  int* counters;
+  const int* runs;
   float* partial;
 };
 
-// Host-side launchers (each returns cudaSuccess or the launch error).
-cudaError_t prepare_plan_kernels();   // once per device, before the first launch
-cudaError_t launch_plan(const PlanArgs& a, int num_sms, cudaStream_t stream);
+// Host-side launchers.
+cudaError_t prepare_kernels();   // once per device, before the first launch
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+// apply_long then apply_rest, each chained to its predecessor by programmatic
+// dependent launch.
 cudaError_t launch_apply(const ApplyArgs& a, int grad_bf16, int mg_bf16, int num_sms,
                          cudaStream_t stream);
 

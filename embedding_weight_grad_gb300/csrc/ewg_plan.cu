@@ -2,23 +2,29 @@
 //
 // Counterpart of _sort_tokens_kernel (Megatron Core API docs,
 // core.fusions.fused_embedding_wgrad, "Functions"): sort the (token, position) pairs,
-// find every sorted slot's run, list the chunks of at most NROWS slots.
+// give every sorted slot its run, list the chunks of at most NROWS slots and the runs
+// longer than NROWS.
 //
-// The sort is an LSD radix sort over the id bits only.  Keys arrive in position
-// order and every pass is stable, so positions stay ascending inside each run
-// without passes of their own.  Up to 8192 tokens one CTA does everything in
-// shared memory; above that the passes run as histogram / scan / scatter kernels
-// over tiles of 2048 keys.
+// Sorting is an LSD radix sort over the id bits only.  Keys arrive in position order
+// and every pass is stable, so positions stay ascending inside each run without passes
+// of their own.
+//
+// Up to 8192 tokens (hashed path): 64 CTAs each read all ids and keep the ids of one
+// hash partition (id * golden-ratio constant, top 6 bits), in position order; each
+// CTA then sorts and lists its partition alone in shared memory.  A run never spans
+// two partitions, so no CTA waits for another, and the apply kernels find each
+// partition's lists through the partition tables.
+//
+// Above 8192 tokens (multi-tile path): histogram / scan / scatter kernels over tiles
+// of 2048 keys per radix pass, then count / scan / emit kernels for the listing.
 //
 // The listing gives every sorted slot s its run's first slot rs and last slot re.
-// Slot s starts a chunk when (s - rs) % NROWS == 0; chunks are numbered by a scan
-// in slot order, and chunks of runs longer than NROWS also get a row of the fp32
-// partial-sum buffer.  Each chunk is written as a 64-byte descriptor that carries
-// its token positions, so the apply kernel needs no further indirection.
+// Slot s starts a chunk when (s - rs) % NROWS == 0.
 #include <climits>
 
 #include "ewg.h"
 #include "ewg_internal.cuh"
+#include "ewg_ptx.cuh"
 
 namespace ewg {
 namespace {
@@ -35,8 +41,11 @@ struct MinOp {
 struct SumOp {
   __device__ long long operator()(long long a, long long b) const { return a + b; }
 };
+struct SumIntOp {
+  __device__ int operator()(int a, int b) const { return a + b; }
+};
 
-// Exclusive prefix scan over the block in thread order.  `sw` needs NW entries.
+// Exclusive prefix scan over the block in thread order.  `sw` needs NT/32 entries.
 template <int NT, typename T, typename Op>
 __device__ T block_exclusive_scan(T v, Op op, T ident, T* sw, T* total) {
   constexpr int NW = NT / 32;
@@ -50,13 +59,13 @@ __device__ T block_exclusive_scan(T v, Op op, T ident, T* sw, T* total) {
   if (lane == 31) sw[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    T a = lane < NW ? sw[lane] : ident;
+    T s = lane < NW ? sw[lane] : ident;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      T y = __shfl_up_sync(kFull, a, o);
-      if (lane >= o) a = op(y, a);
+      T y = __shfl_up_sync(kFull, s, o);
+      if (lane >= o) s = op(y, s);
     }
-    if (lane < NW) sw[lane] = a;
+    if (lane < NW) sw[lane] = s;
   }
   __syncthreads();
   T before_warp = warp > 0 ? sw[warp - 1] : ident;
@@ -81,13 +90,13 @@ __device__ T block_exclusive_suffix_scan(T v, Op op, T ident, T* sw) {
   if (lane == 0) sw[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    T a = lane < NW ? sw[lane] : ident;
+    T s = lane < NW ? sw[lane] : ident;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      T y = __shfl_down_sync(kFull, a, o);
-      if (lane + o < 32) a = op(a, y);
+      T y = __shfl_down_sync(kFull, s, o);
+      if (lane + o < 32) s = op(s, y);
     }
-    if (lane < NW) sw[lane] = a;
+    if (lane < NW) sw[lane] = s;
   }
   __syncthreads();
   T after_warp = warp + 1 < NW ? sw[warp + 1] : ident;
@@ -98,21 +107,20 @@ __device__ T block_exclusive_suffix_scan(T v, Op op, T ident, T* sw) {
 }
 
 template <int NT>
-__device__ int block_sum_int(int v, long long* sw64) {
+__device__ long long block_sum(long long v, long long* sw64) {
   long long tot = 0;
-  block_exclusive_scan<NT, long long>(static_cast<long long>(v), SumOp(), 0ll, sw64, &tot);
-  return static_cast<int>(tot);
+  block_exclusive_scan<NT, long long>(v, SumOp(), 0ll, sw64, &tot);
+  return tot;
 }
 
 __device__ __forceinline__ long long load_id(const void* ids, int is64, int i) {
   return is64 ? static_cast<const long long*>(ids)[i] : static_cast<const int*>(ids)[i];
 }
 
-// Validated sort key of token i: the id, 0 for an out-of-range id (the call is then
-// void anyway), kPadKey past the end.
+// Validated sort key of token i: the id; 0 for an out-of-range id (the call is then
+// void anyway).
 __device__ __forceinline__ uint32_t make_key(const PlanArgs& a, int i, int& bad) {
-  if (i >= a.n) return kPadKey;
-  long long id = load_id(a.ids, a.ids_int64, i);
+  const long long id = load_id(a.ids, a.ids_int64, i);
   if (id < 0 || id >= a.num_embeddings) {
     ++bad;
     return 0u;
@@ -150,10 +158,24 @@ __device__ int warp_bound(const uint32_t* keys, int lo, int hi, uint32_t k, bool
   return min(lo + f, hi);
 }
 
-// ---------------------------------------------------------------------------
+// Per-thread counts packed in one 64-bit word, 21 bits per field (block-local counts
+// stay below 2^21): short chunks << 42 | long chunks << 21 | long runs.
+constexpr int kField = 21;
+constexpr long long kFieldMask = (1ll << kField) - 1;
+__device__ __forceinline__ int field_short(long long p) { return static_cast<int>(p >> (2 * kField)); }
+__device__ __forceinline__ int field_long(long long p) { return static_cast<int>((p >> kField) & kFieldMask); }
+__device__ __forceinline__ int field_runs(long long p) { return static_cast<int>(p & kFieldMask); }
+
+struct EmitBases {
+  int long_desc;     // descriptor index of the first long chunk
+  int short_desc;    // descriptor index of the first short chunk
+  int partial;       // partial row of the first long chunk
+  int run;           // long-run table index of the first long run
+};
+
 // Listing of one block of slots [s_begin, s_begin + NT*ITEMS), thread-blocked.
 // rs_seed: first slot of the run of slot s_begin; re_seed: last slot of the run of
-// the block's last valid slot.  Produces per-item run bounds in registers.
+// the block's last valid slot.
 template <int NT, int ITEMS>
 struct Listing {
   int rs[ITEMS];
@@ -178,8 +200,8 @@ struct Listing {
         if (tail[i]) tmin = min(tmin, s);
       }
     }
-    int before = block_exclusive_scan<NT, int>(hmax, MaxOp(), -1, swi, nullptr);
-    int after = block_exclusive_suffix_scan<NT, int>(tmin, MinOp(), INT_MAX, swi);
+    const int before = block_exclusive_scan<NT, int>(hmax, MaxOp(), -1, swi, nullptr);
+    const int after = block_exclusive_suffix_scan<NT, int>(tmin, MinOp(), INT_MAX, swi);
     int cur = max(before, rs_seed);
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
@@ -194,7 +216,6 @@ struct Listing {
     }
   }
 
-  // Per-thread chunk-head counts packed as (chunks << 32) | long_chunks.
   __device__ long long counts(int n, int s_begin) const {
     const int base = s_begin + threadIdx.x * ITEMS;
     long long c = 0;
@@ -202,146 +223,237 @@ struct Listing {
     for (int i = 0; i < ITEMS; ++i) {
       const int s = base + i;
       if (s < n && (s - rs[i]) % kNrows == 0) {
-        c += 1ll << 32;
-        if (re[i] - rs[i] + 1 > kNrows) c += 1;
+        if (re[i] - rs[i] + 1 > kNrows) {
+          c += 1ll << kField;
+          if (s == rs[i]) c += 1;
+        } else {
+          c += 1ll << (2 * kField);
+        }
       }
     }
     return c;
   }
 
-  // Writes the descriptors of the chunks that start in this thread's slots.
-  __device__ void emit(const PlanArgs& a, const uint32_t* vals, int s_begin,
-                       long long prefix) const {
+  // Writes the descriptors of the chunks that start in this thread's slots; `prefix`
+  // is the packed count of the chunks and runs before this thread's slots.
+  __device__ void emit(const PlanArgs& a, const uint32_t* vals, int n, int s_begin,
+                       long long prefix, const EmitBases& b) const {
     const int base = s_begin + threadIdx.x * ITEMS;
-    int ci = static_cast<int>(prefix >> 32);
-    int lc = static_cast<int>(prefix & 0xffffffffll);
+    int si = field_short(prefix), li = field_long(prefix), ri = field_runs(prefix);
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int s = base + i;
-      if (s >= a.n || (s - rs[i]) % kNrows != 0) continue;
+      if (s >= n || (s - rs[i]) % kNrows != 0) continue;
       const int L = re[i] - rs[i] + 1;
       const int c = (s - rs[i]) / kNrows;
       const int len = min(kNrows, re[i] - s + 1);
+      const int C = (L + kNrows - 1) / kNrows;
       const bool is_long = L > kNrows;
-      int4* d = reinterpret_cast<int4*>(a.chunks + static_cast<long long>(ci) * kChunkWords);
+      const int desc = is_long ? b.long_desc + li : b.short_desc + si;
+      const int prow = is_long ? b.partial + li : -1;
+      int4* d = reinterpret_cast<int4*>(a.chunks + static_cast<long long>(desc) * kChunkWords);
       int p[kNrows];
 #pragma unroll
       for (int k = 0; k < kNrows; ++k) p[k] = k < len ? static_cast<int>(vals[s + k]) : 0;
       d[0] = make_int4(p[0], p[1], p[2], p[3]);
       d[1] = make_int4(p[4], p[5], p[6], p[7]);
       d[2] = make_int4(p[8], p[9], static_cast<int>(key[i]), len | (c << 4));
-      d[3] = make_int4(is_long ? lc : -1, (L + kNrows - 1) / kNrows, 0, 0);
-      if (is_long && c == 0) {
-        int* cnt = a.counters + static_cast<long long>(lc) * a.slices;
-        for (int j = 0; j < a.slices; ++j) cnt[j] = 0;
+      d[3] = make_int4(prow, C, 0, 0);
+      if (is_long) {
+        if (c == 0) {
+          reinterpret_cast<int4*>(a.runs)[b.run + ri] = make_int4(prow, C, static_cast<int>(key[i]), 0);
+          ++ri;
+        }
+        ++li;
+      } else {
+        ++si;
       }
-      ++ci;
-      if (is_long) ++lc;
     }
   }
 };
 
-__device__ void write_header(const PlanArgs& a, int chunks, int long_chunks, int bad) {
+__device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
   Header* h = a.header;
-  h->num_chunks = chunks;
-  h->num_long_chunks = long_chunks;
-  h->bad_ids = bad;
   h->n = a.n;
   h->hidden = a.hidden;
   h->num_embeddings = a.num_embeddings;
+  h->num_parts = num_parts;
+  h->bad_ids = bad;
   h->status = bad ? EWG_ERR_ID_OUT_OF_RANGE : EWG_OK;
 }
 
-// ---------------------------------------------------------------------------
-// Single-CTA plan for n <= 8192: keys live in shared memory throughout.
+__device__ void write_tables(const PlanArgs& a, int part, int long_cnt, int long_off,
+                             int short_cnt, int short_off, int run_cnt, int run_off) {
+  a.tables[kLongCnt * kMaxParts + part] = long_cnt;
+  a.tables[kLongOff * kMaxParts + part] = long_off;
+  a.tables[kShortCnt * kMaxParts + part] = short_cnt;
+  a.tables[kShortOff * kMaxParts + part] = short_off;
+  a.tables[kRunCnt * kMaxParts + part] = run_cnt;
+  a.tables[kRunOff * kMaxParts + part] = run_off;
+}
 
-constexpr size_t kSmallSmem =
-    static_cast<size_t>(4) * kSmallMaxN * 4 + static_cast<size_t>(1 << kMaxDigitBits) * 32 * 4;
-
-__global__ void __launch_bounds__(kSmallThreads, 1) plan_small_kernel(PlanArgs a) {
-  extern __shared__ __align__(16) uint32_t sm[];
-  uint32_t* ks = sm;
-  uint32_t* vs = ks + kSmallMaxN;
-  uint32_t* kd = vs + kSmallMaxN;
-  uint32_t* vd = kd + kSmallMaxN;
-  uint32_t* cnt = vd + kSmallMaxN;   // [bucket][warp]
-  __shared__ long long sw64[32];
-  __shared__ int swi[32];
+// Stable LSD radix sort of m (key, value) pairs in shared memory by the id bits.  Warp w
+// ranks the contiguous key range [w*K, (w+1)*K) in (round, lane) order; counters are laid
+// out [warp][bucket] so that the lanes of one warp hit distinct banks.
+template <int NT, int MAXR>
+__device__ void smem_radix_sort(uint32_t*& ks, uint32_t*& vs, uint32_t*& kd, uint32_t*& vd, int m,
+                                const PlanArgs& a, uint32_t* cnt, long long* sw64) {
+  constexpr int NW = NT / 32;
+  constexpr int kStride = 1 << kMaxDigitBits;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  constexpr int NW = kSmallThreads / 32;
-
-  int bad = 0;
-#pragma unroll
-  for (int r = 0; r < kSmallItems; ++r) {
-    const int i = r * kSmallThreads + t;
-    ks[i] = make_key(a, i, bad);
-    vs[i] = static_cast<uint32_t>(i);
-  }
-  bad = block_sum_int<kSmallThreads>(bad, sw64);
-
+  const int K = ((m + NW - 1) / NW + 31) / 32 * 32;
+  const int rounds = K / 32;
+  const int w0 = warp * K;
+  const uint32_t lt = (1u << lane) - 1u;
   for (int pass = 0; pass < a.passes; ++pass) {
     const int sh = pass * a.digit_bits;
     const int bits = min(a.digit_bits, a.id_bits - sh);
     const uint32_t B = 1u << bits, mask = B - 1;
-    for (uint32_t i = t; i < B * NW; i += kSmallThreads) cnt[i] = 0;
+    for (uint32_t i = t; i < NW * B; i += NT) cnt[(i / B) * kStride + (i % B)] = 0;
     __syncthreads();
-    uint32_t key[kSmallItems], val[kSmallItems], rank[kSmallItems], dig[kSmallItems];
-    // warp w ranks its 256 keys in (round, lane) order, which is input order
+    uint32_t rank[MAXR], dig[MAXR];
 #pragma unroll
-    for (int r = 0; r < kSmallItems; ++r) {
-      const int idx = warp * (32 * kSmallItems) + r * 32 + lane;
-      key[r] = ks[idx];
-      val[r] = vs[idx];
-      const uint32_t d = (key[r] >> sh) & mask;
-      const unsigned peers = __match_any_sync(kFull, d);
-      const uint32_t below = __popc(peers & ((1u << lane) - 1u));
-      const uint32_t prior = cnt[d * NW + warp];
-      __syncwarp();
-      if (lane == 31 - __clz(peers)) cnt[d * NW + warp] = prior + __popc(peers);
-      __syncwarp();
-      rank[r] = prior + below;
-      dig[r] = d;
+    for (int r = 0; r < MAXR; ++r) {
+      rank[r] = 0;
+      dig[r] = 0;
+      if (r < rounds) {
+        const int idx = w0 + r * 32 + lane;
+        const bool valid = idx < m;
+        const uint32_t d = valid ? (ks[idx] >> sh) & mask : 0xffffffffu;
+        const unsigned peers = __match_any_sync(kFull, d);
+        uint32_t prior = 0;
+        if (valid) prior = cnt[warp * kStride + d];
+        __syncwarp();
+        if (valid && lane == 31 - __clz(peers)) cnt[warp * kStride + d] = prior + __popc(peers);
+        __syncwarp();
+        rank[r] = prior + __popc(peers & lt);
+        dig[r] = d;
+      }
     }
     __syncthreads();
-    // exclusive scan of cnt in (bucket, warp) order
-    {
-      const int E = static_cast<int>(B) * NW;
-      const int per = (E + kSmallThreads - 1) / kSmallThreads;
-      const int b0 = min(E, t * per), b1 = min(E, b0 + per);
-      long long local = 0;
-      for (int i = b0; i < b1; ++i) local += cnt[i];
-      long long run = block_exclusive_scan<kSmallThreads, long long>(local, SumOp(), 0ll, sw64,
-                                                                    nullptr);
-      for (int i = b0; i < b1; ++i) {
-        const uint32_t c = cnt[i];
-        cnt[i] = static_cast<uint32_t>(run);
+    uint32_t tot = 0;
+    if (t < static_cast<int>(B))
+      for (int w = 0; w < NW; ++w) tot += cnt[w * kStride + t];
+    long long run = block_exclusive_scan<NT, long long>(tot, SumOp(), 0ll, sw64, nullptr);
+    if (t < static_cast<int>(B)) {
+      for (int w = 0; w < NW; ++w) {
+        const uint32_t c = cnt[w * kStride + t];
+        cnt[w * kStride + t] = static_cast<uint32_t>(run);
         run += c;
       }
     }
     __syncthreads();
 #pragma unroll
-    for (int r = 0; r < kSmallItems; ++r) {
-      const uint32_t dst = cnt[dig[r] * NW + warp] + rank[r];
-      kd[dst] = key[r];
-      vd[dst] = val[r];
+    for (int r = 0; r < MAXR; ++r) {
+      if (r < rounds) {
+        const int idx = w0 + r * 32 + lane;
+        if (idx < m) {
+          const uint32_t dst = cnt[warp * kStride + dig[r]] + rank[r];
+          kd[dst] = ks[idx];
+          vd[dst] = vs[idx];
+        }
+      }
     }
     __syncthreads();
     uint32_t* tk = ks; ks = kd; kd = tk;
     uint32_t* tv = vs; vs = vd; vd = tv;
   }
+}
 
-  Listing<kSmallThreads, kSmallItems> L;
-  L.compute(ks, a.n, 0, 0, a.n - 1, swi);
-  long long total = 0;
-  long long prefix = block_exclusive_scan<kSmallThreads, long long>(L.counts(a.n, 0), SumOp(),
-                                                                   0ll, sw64, &total);
-  if (!bad) L.emit(a, vs, 0, prefix);
-  if (t == 0) write_header(a, static_cast<int>(total >> 32),
-                           static_cast<int>(total & 0xffffffffll), bad);
+__device__ __forceinline__ int hash_part(uint32_t id) {
+  static_assert(kHashParts == 64, "hash uses the top 6 bits");
+  return static_cast<int>((id * 0x9E3779B1u) >> 26);
+}
+
+constexpr int kHashWarps = kHashThreads / 32;
+constexpr size_t kHashSmem = static_cast<size_t>(4) * kHashMaxN * 4 +
+                             static_cast<size_t>(kHashWarps) * (1 << kMaxDigitBits) * 4;
+
+// ---------------------------------------------------------------------------
+// Hashed plan: CTA b handles the ids whose hash partition is b.
+
+__global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a) {
+  ptx::pdl_launch_dependents();
+  extern __shared__ __align__(16) uint32_t sm[];
+  uint32_t* ks = sm;
+  uint32_t* vs = ks + kHashMaxN;
+  uint32_t* kd = vs + kHashMaxN;
+  uint32_t* vd = kd + kHashMaxN;
+  uint32_t* cnt = vd + kHashMaxN;
+  __shared__ int wc[kHashItems * kHashWarps];
+  __shared__ long long sw64[kHashWarps];
+  __shared__ int swi[kHashWarps];
+  const int part = blockIdx.x;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+
+  // 1. every id, striped: round r covers positions [r*NT, (r+1)*NT)
+  uint32_t key[kHashItems];
+  unsigned ballot[kHashItems];
+  int bad = 0, before = 0;
+#pragma unroll
+  for (int r = 0; r < kHashItems; ++r) {
+    const int p = r * kHashThreads + t;
+    bool mine = false;
+    key[r] = 0;
+    if (p < a.n) {
+      key[r] = make_key(a, p, bad);
+      const int h = hash_part(key[r]);
+      mine = h == part;
+      before += h < part;
+    }
+    ballot[r] = __ballot_sync(kFull, mine);
+    if (lane == 0) wc[r * kHashWarps + warp] = __popc(ballot[r]);
+  }
+  const long long red = block_sum<kHashThreads>((static_cast<long long>(bad) << 32) | before, sw64);
+  const int bad_total = static_cast<int>(red >> 32);
+  const int S_b = static_cast<int>(red & 0xffffffffll);   // tokens of partitions < part
+  if (bad_total) {
+    if (part == 0 && t == 0) write_header(a, kHashParts, bad_total);
+    return;
+  }
+
+  // 2. this partition's (id, position) pairs, compacted in position order
+  int total = 0;
+  {
+    const int v = t < kHashItems * kHashWarps ? wc[t] : 0;
+    const int off = block_exclusive_scan<kHashThreads, int>(v, SumIntOp(), 0, swi, &total);
+    if (t < kHashItems * kHashWarps) wc[t] = off;
+    __syncthreads();
+  }
+#pragma unroll
+  for (int r = 0; r < kHashItems; ++r) {
+    if ((ballot[r] >> lane) & 1u) {
+      const int slot = wc[r * kHashWarps + warp] + __popc(ballot[r] & lt);
+      ks[slot] = key[r];
+      vs[slot] = static_cast<uint32_t>(r * kHashThreads + t);
+    }
+  }
+  __syncthreads();
+  const int m = total;
+
+  // 3. sort by id, 4. list runs and chunks
+  smem_radix_sort<kHashThreads, kHashItems>(ks, vs, kd, vd, m, a, cnt, sw64);
+  Listing<kHashThreads, kHashItems> L;
+  L.compute(ks, m, 0, 0, m - 1, swi);
+  long long tot = 0;
+  const long long prefix =
+      block_exclusive_scan<kHashThreads, long long>(L.counts(m, 0), SumOp(), 0ll, sw64, &tot);
+  const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
+  EmitBases eb;
+  eb.long_desc = S_b;
+  eb.short_desc = S_b + n_long;
+  eb.partial = (2 * S_b) / 11 + part;
+  eb.run = S_b / 11 + part;
+  L.emit(a, vs, m, 0, prefix, eb);
+  if (t == 0) {
+    write_tables(a, part, n_long, eb.long_desc, n_short, eb.short_desc, n_runs, eb.run);
+    if (part == 0) write_header(a, kHashParts, 0);
+  }
 }
 
 // ---------------------------------------------------------------------------
-// Multi-CTA plan: tiles of kTile keys, one CTA each.
+// Multi-tile plan: tiles of kTile keys, one CTA each.
 
 // Keys of the tile into the ping buffer, plus the pass-0 digit histogram.
 __global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
@@ -354,12 +466,12 @@ __global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
   int bad = 0;
   for (int r = 0; r < kTileItems; ++r) {
     const int i = tile * kTile + r * kTileThreads + t;
-    const uint32_t k = make_key(a, i, bad);
+    const uint32_t k = i < a.n ? make_key(a, i, bad) : kPadKey;
     a.keys_a[i] = k;
     a.vals_a[i] = static_cast<uint32_t>(i);
     if (B) atomicAdd(&h[k & (B - 1)], 1u);
   }
-  bad = block_sum_int<kTileThreads>(bad, sw64);
+  bad = static_cast<int>(block_sum<kTileThreads>(bad, sw64));
   __syncthreads();
   for (int d = t; d < B; d += kTileThreads) a.hist[static_cast<long long>(d) * a.tiles + tile] = h[d];
   if (t == 0) a.tile_bad[tile] = bad;
@@ -406,44 +518,43 @@ __global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const
                                                                const uint32_t* vs, uint32_t* kd,
                                                                uint32_t* vd, int pass) {
   constexpr int NW = kTileThreads / 32;
-  __shared__ uint32_t cnt[(1 << kMaxDigitBits) * NW];   // [bucket][warp]
+  constexpr int kStride = 1 << kMaxDigitBits;
+  __shared__ uint32_t cnt[NW * kStride];   // [warp][bucket]
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, tile = blockIdx.x;
   const int sh = pass * a.digit_bits;
   const uint32_t B = 1u << min(a.digit_bits, a.id_bits - sh), mask = B - 1;
-  for (uint32_t i = t; i < B * NW; i += kTileThreads) cnt[i] = 0;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (uint32_t i = t; i < NW * B; i += kTileThreads) cnt[(i / B) * kStride + (i % B)] = 0;
   __syncthreads();
-  uint32_t key[kTileItems], val[kTileItems], rank[kTileItems], dig[kTileItems];
+  uint32_t rank[kTileItems], dig[kTileItems];
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
     const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
-    key[r] = ks[idx];
-    val[r] = vs[idx];
-    const uint32_t d = (key[r] >> sh) & mask;
+    const uint32_t d = (ks[idx] >> sh) & mask;
     const unsigned peers = __match_any_sync(kFull, d);
-    const uint32_t below = __popc(peers & ((1u << lane) - 1u));
-    const uint32_t prior = cnt[d * NW + warp];
+    const uint32_t prior = cnt[warp * kStride + d];
     __syncwarp();
-    if (lane == 31 - __clz(peers)) cnt[d * NW + warp] = prior + __popc(peers);
+    if (lane == 31 - __clz(peers)) cnt[warp * kStride + d] = prior + __popc(peers);
     __syncwarp();
-    rank[r] = prior + below;
+    rank[r] = prior + __popc(peers & lt);
     dig[r] = d;
   }
   __syncthreads();
-  // per bucket: offsets of the warps inside the tile, plus the tile's global base
   for (uint32_t d = t; d < B; d += kTileThreads) {
     uint32_t run = a.hist[static_cast<long long>(d) * a.tiles + tile];
     for (int w = 0; w < NW; ++w) {
-      const uint32_t c = cnt[d * NW + w];
-      cnt[d * NW + w] = run;
+      const uint32_t c = cnt[w * kStride + d];
+      cnt[w * kStride + d] = run;
       run += c;
     }
   }
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
-    const uint32_t dst = cnt[dig[r] * NW + warp] + rank[r];
-    kd[dst] = key[r];
-    vd[dst] = val[r];
+    const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
+    const uint32_t dst = cnt[warp * kStride + dig[r]] + rank[r];
+    kd[dst] = ks[idx];
+    vd[dst] = vs[idx];
   }
 }
 
@@ -473,37 +584,48 @@ __global__ void __launch_bounds__(kTileThreads) list_count_kernel(PlanArgs a,
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
-  long long total = 0;
-  block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0), SumOp(), 0ll, sw64, &total);
-  if (threadIdx.x == 0) a.tile_cnt[blockIdx.x] = total;
+  const long long tot = block_sum<kTileThreads>(L.counts(a.n, s0), sw64);
+  if (threadIdx.x == 0)
+    a.tile_cnt[blockIdx.x] = make_int4(field_long(tot), field_short(tot), field_runs(tot), 0);
 }
 
-// Scans the per-tile chunk counts, sums the bad-id counts and writes the header.
+// Scans the per-tile counts, sums the bad-id counts, writes the header and the
+// (single-partition) tables.
 __global__ void __launch_bounds__(1024) list_scan_kernel(PlanArgs a) {
   __shared__ long long sw64[32];
   const int t = threadIdx.x;
   const int per = (a.tiles + 1023) / 1024;
   const int b0 = min(a.tiles, t * per), b1 = min(a.tiles, b0 + per);
-  long long local = 0;
-  int bad = 0;
+  long long l = 0, s = 0, r = 0, bad = 0;
   for (int i = b0; i < b1; ++i) {
-    local += a.tile_cnt[i];
+    const int4 c = a.tile_cnt[i];
+    l += c.x;
+    s += c.y;
+    r += c.z;
     bad += a.tile_bad[i];
   }
-  long long total = 0;
-  long long run = block_exclusive_scan<1024, long long>(local, SumOp(), 0ll, sw64, &total);
+  long long tl = 0, ts = 0, tr = 0;
+  long long pl = block_exclusive_scan<1024, long long>(l, SumOp(), 0ll, sw64, &tl);
+  long long ps = block_exclusive_scan<1024, long long>(s, SumOp(), 0ll, sw64, &ts);
+  long long pr = block_exclusive_scan<1024, long long>(r, SumOp(), 0ll, sw64, &tr);
   for (int i = b0; i < b1; ++i) {
-    const long long c = a.tile_cnt[i];
-    a.tile_cnt[i] = run;
-    run += c;
+    const int4 c = a.tile_cnt[i];
+    a.tile_cnt[i] = make_int4(static_cast<int>(pl), static_cast<int>(ps), static_cast<int>(pr), 0);
+    pl += c.x;
+    ps += c.y;
+    pr += c.z;
   }
-  bad = block_sum_int<1024>(bad, sw64);
-  if (t == 0) write_header(a, static_cast<int>(total >> 32), static_cast<int>(total & 0xffffffffll),
-                           bad);
+  const long long bad_total = block_sum<1024>(bad, sw64);
+  if (t == 0) {
+    write_tables(a, 0, static_cast<int>(tl), 0, static_cast<int>(ts), static_cast<int>(tl),
+                 static_cast<int>(tr), 0);
+    write_header(a, 1, static_cast<int>(bad_total));
+  }
 }
 
 __global__ void __launch_bounds__(kTileThreads) list_emit_kernel(PlanArgs a, const uint32_t* keys,
                                                                  const uint32_t* vals) {
+  ptx::pdl_launch_dependents();
   __shared__ int swi[kTileThreads / 32];
   __shared__ long long sw64[kTileThreads / 32];
   if (a.header->status != EWG_OK) return;
@@ -512,23 +634,28 @@ __global__ void __launch_bounds__(kTileThreads) list_emit_kernel(PlanArgs a, con
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
-  long long prefix = block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0), SumOp(), 0ll,
-                                                                  sw64, nullptr);
-  L.emit(a, vals, s0, prefix + a.tile_cnt[blockIdx.x]);
+  const long long prefix =
+      block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0), SumOp(), 0ll, sw64, nullptr);
+  const int4 tp = a.tile_cnt[blockIdx.x];
+  EmitBases eb;
+  eb.long_desc = tp.x;
+  eb.short_desc = a.tables[kLongCnt * kMaxParts] + tp.y;
+  eb.partial = tp.x;
+  eb.run = tp.z;
+  L.emit(a, vals, a.n, s0, prefix, eb);
 }
 
 }  // namespace
 
-cudaError_t prepare_plan_kernels() {
-  static_assert(kSmallSmem <= 227 * 1024, "single-CTA plan must fit in shared memory");
-  return cudaFuncSetAttribute(plan_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kSmallSmem));
+cudaError_t prepare_kernels() {
+  static_assert(kHashSmem <= 227 * 1024, "hashed plan must fit in shared memory");
+  return cudaFuncSetAttribute(plan_hashed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kHashSmem));
 }
 
-cudaError_t launch_plan(const PlanArgs& a, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
-  if (a.n <= kSmallMaxN) {
-    plan_small_kernel<<<1, kSmallThreads, kSmallSmem, stream>>>(a);
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
+  if (a.n <= kHashMaxN) {
+    plan_hashed_kernel<<<kHashParts, kHashThreads, kHashSmem, stream>>>(a);
     return cudaGetLastError();
   }
   const int tiles = a.tiles;

@@ -66,6 +66,8 @@ extern "C" {
 #define EWG_ERR_INVALID 2         /* bad argument: NULL, size, workspace too small, plan mismatch */
 #define EWG_ERR_CUDA 3            /* a CUDA runtime call or kernel launch failed */
 #define EWG_ERR_ID_OUT_OF_RANGE 4 /* device-detected: an id outside [0, num_embeddings) */
+#define EWG_ERR_TIMEOUT 5         /* device-detected: a bounded wait in a kernel gave up;
+                                     touched main_grad rows are then unspecified */
 
 /*
  * Whether ewg_accumulate supports these tensors (can_accumulate_embedding_wgrad on
@@ -132,8 +134,8 @@ int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_emb
 
 /*
  * The second half of ewg_accumulate (the page's _partial_sums_kernel and
- * _long_run_sums_kernel, as one kernel): sums the chunks of the plan in the
- * workspace and adds each token's row into main_grad.  num_tokens, num_embeddings
+ * _long_run_sums_kernel): sums the chunks of the plan in the workspace and adds
+ * each token's row into main_grad.  num_tokens, num_embeddings
  * and hidden must be those given to the ewg_plan that filled the workspace (the
  * kernel checks them against the plan and writes nothing on a mismatch, reporting
  * EWG_ERR_INVALID through ewg_read_status).  Must be ordered after that ewg_plan.
@@ -146,7 +148,8 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride,
 /*
  * Waits for `stream`, then copies the device status of the last ewg_plan /
  * ewg_apply / ewg_accumulate that used this workspace into *status (EWG_OK,
- * EWG_ERR_ID_OUT_OF_RANGE or EWG_ERR_INVALID).  Returns EWG_OK or EWG_ERR_CUDA.
+ * EWG_ERR_ID_OUT_OF_RANGE, EWG_ERR_INVALID or EWG_ERR_TIMEOUT).  Returns EWG_OK or
+ * EWG_ERR_CUDA.
  */
 int ewg_read_status(const void* workspace, void* stream, int* status);
 
