@@ -340,23 +340,35 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int list = LONG ? 0 : 1;
   const long long n_items = static_cast<long long>(s.prefix[list][parts]) * T;
   int cur = 0;
-  // two descriptors in flight ahead of the item being issued
-  long long o0 = idx, o1 = idx + G;
-  Desc d0{}, d1{};
-  if (o0 < n_items) d0 = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
-                                                        static_cast<int>(o0 / T), cur));
-  if (o1 < n_items) d1 = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
-                                                        static_cast<int>(o1 / T), cur));
-  while (o0 < n_items && P.ok) {
-    const long long o2 = o1 + G;
-    Desc d2{};
-    if (o2 < n_items) d2 = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
-                                                          static_cast<int>(o2 / T), cur));
-    P.ok = P.chunk_item(d0, static_cast<int>(o0 % T));
-    o0 = o1;
-    d0 = d1;
-    o1 = o2;
-    d1 = d2;
+  // A ring of kAhead descriptors loaded kAhead items ahead.  The loop over the ring is
+  // unrolled so that every slot keeps its own registers: copying a register whose load
+  // is still in flight would stall the producer on that load.
+  constexpr int kAhead = 4;
+  Desc d[kAhead];
+  long long o[kAhead];
+#pragma unroll
+  for (int j = 0; j < kAhead; ++j) {
+    o[j] = idx + j * G;
+    if (o[j] < n_items)
+      d[j] = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
+                                            static_cast<int>(o[j] / T), cur));
+  }
+  bool more = o[0] < n_items;
+  while (more && P.ok) {
+#pragma unroll
+    for (int j = 0; j < kAhead; ++j) {
+      if (more && P.ok) {
+        if (o[j] >= n_items) {
+          more = false;
+        } else {
+          P.ok = P.chunk_item(d[j], static_cast<int>(o[j] % T));
+          o[j] += kAhead * G;
+          if (o[j] < n_items)
+            d[j] = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
+                                                  static_cast<int>(o[j] / T), cur));
+        }
+      }
+    }
   }
   P.finish_stream();
 }

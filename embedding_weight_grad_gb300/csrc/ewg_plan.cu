@@ -117,17 +117,6 @@ __device__ __forceinline__ long long load_id(const void* ids, int is64, int i) {
   return is64 ? static_cast<const long long*>(ids)[i] : static_cast<const int*>(ids)[i];
 }
 
-// Validated sort key of token i: the id; 0 for an out-of-range id (the call is then
-// void anyway).
-__device__ __forceinline__ uint32_t make_key(const PlanArgs& a, int i, int& bad) {
-  const long long id = load_id(a.ids, a.ids_int64, i);
-  if (id < 0 || id >= a.num_embeddings) {
-    ++bad;
-    return 0u;
-  }
-  return static_cast<uint32_t>(id);
-}
-
 // Warp-wide 32-ary search in a sorted key array: first index in [lo, hi) whose key
 // is >= k (upper == false) or > k (upper == true); hi if there is none.
 __device__ int warp_bound(const uint32_t* keys, int lo, int hi, uint32_t k, bool upper) {
@@ -387,7 +376,14 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t lt = (1u << lane) - 1u;
 
-  // 1. every id, striped: round r covers positions [r*NT, (r+1)*NT)
+  // 1. every id, striped: round r covers positions [r*NT, (r+1)*NT).  All loads are
+  // issued before any is used, so they overlap.
+  long long raw[kHashItems];
+#pragma unroll
+  for (int r = 0; r < kHashItems; ++r) {
+    const int p = r * kHashThreads + t;
+    raw[r] = p < a.n ? load_id(a.ids, a.ids_int64, p) : 0;
+  }
   uint32_t key[kHashItems];
   unsigned ballot[kHashItems];
   int bad = 0, before = 0;
@@ -397,7 +393,11 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
     bool mine = false;
     key[r] = 0;
     if (p < a.n) {
-      key[r] = make_key(a, p, bad);
+      if (raw[r] < 0 || raw[r] >= a.num_embeddings) {
+        ++bad;
+      } else {
+        key[r] = static_cast<uint32_t>(raw[r]);
+      }
       const int h = hash_part(key[r]);
       mine = h == part;
       before += h < part;
@@ -464,9 +464,24 @@ __global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
   for (int i = t; i < B; i += kTileThreads) h[i] = 0;
   __syncthreads();
   int bad = 0;
+  long long raw[kTileItems];
+#pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
     const int i = tile * kTile + r * kTileThreads + t;
-    const uint32_t k = i < a.n ? make_key(a, i, bad) : kPadKey;
+    raw[r] = i < a.n ? load_id(a.ids, a.ids_int64, i) : 0;
+  }
+#pragma unroll
+  for (int r = 0; r < kTileItems; ++r) {
+    const int i = tile * kTile + r * kTileThreads + t;
+    uint32_t k = kPadKey;
+    if (i < a.n) {
+      if (raw[r] < 0 || raw[r] >= a.num_embeddings) {
+        ++bad;
+        k = 0u;
+      } else {
+        k = static_cast<uint32_t>(raw[r]);
+      }
+    }
     a.keys_a[i] = k;
     a.vals_a[i] = static_cast<uint32_t>(i);
     if (B) atomicAdd(&h[k & (B - 1)], 1u);
