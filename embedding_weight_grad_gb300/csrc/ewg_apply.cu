@@ -216,9 +216,10 @@ struct Producer {
   // Publishes item info and arms the slot's barrier for `bytes` of copies.
   __device__ uint64_t* open(const Item& it, uint32_t bytes) {
     const int slot = q % kSlots;
+    // The consumers' reads of this ring space are ordered before these copies by the
+    // slot's empty barrier, which the producer has waited on.
     s.info[slot] = it;
     tail = static_cast<uint32_t>(it.off) + bytes;
-    ptx::fence_proxy_async_smem();
     ptx::mbar_arrive_expect_tx(&s.full[slot], bytes);
     ++q;
     return &s.full[slot];
