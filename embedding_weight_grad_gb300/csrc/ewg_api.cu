@@ -180,6 +180,7 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.mg_stride = mg_row_stride;
   a.n = static_cast<int>(n);
   a.hidden = static_cast<int>(H);
+  a.tile_cols = ewg::tile_cols(H, grad_dtype == EWG_BF16);
   a.num_embeddings = V;
   a.header = at<ewg::Header>(ws, L.header);
   a.tables = at<int>(ws, L.tables);

@@ -232,8 +232,8 @@ struct Producer {
   // One (chunk, column tile) item: the chunk's grad row segments, plus the main_grad
   // segment when the run has no other chunk.
   __device__ bool chunk_item(const Desc& d, int tile) {
-    const int col0 = tile * kColTile;
-    const int cols = min(kColTile, a.hidden - col0);
+    const int col0 = tile * a.tile_cols;
+    const int cols = min(a.tile_cols, a.hidden - col0);
     const int meta = d.w[2].w;
     const int len = meta & 15;
     const int id = d.w[2].z;
@@ -320,7 +320,7 @@ template <bool GBF16, bool MBF16, bool LONG>
 __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   Producer<GBF16, MBF16, LONG> P(a, s, ring);
   const int parts = s.num_parts;
-  const int T = static_cast<int>((a.hidden + kColTile - 1) / kColTile);
+  const int T = (a.hidden + a.tile_cols - 1) / a.tile_cols;
   const long long G = gridDim.x;
   long long idx = blockIdx.x;
 
@@ -388,10 +388,10 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
     }
     const Item it = s.info[slot];
     if (it.kind == kEnd) return;
-    const int c = t * 8;
-    if (c < it.cols) {
-      const unsigned char* base = ring + it.off;
-      if (it.kind == kCombine) {
+    const unsigned char* base = ring + it.off;
+    if (it.kind == kCombine) {   // at most kCombineCols <= 8 * kConsumers columns
+      const int c = t * 8;
+      if (c < it.cols) {
         const uint32_t row_bytes = it.cols * 4;
         if (it.flags & 1) {
 #pragma unroll
@@ -401,8 +401,10 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
         if (it.flags & 2)
           finish<GBF16, MBF16>(a, total, base + it.rows * row_bytes + c * (MBF16 ? 2 : 4), it.id,
                                it.col0 + c);
-      } else {
-        const uint32_t row_bytes = it.cols * (GBF16 ? 2 : 4);
+      }
+    } else {   // chunk item: passes of 8 * kConsumers columns over the tile
+      const uint32_t row_bytes = it.cols * (GBF16 ? 2 : 4);
+      for (int c = t * 8; c < it.cols; c += 8 * kConsumers) {
         float part[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) part[e] = 0.0f;
@@ -428,7 +430,7 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
 }
 
 template <bool GBF16, bool MBF16, bool LONG>
-__global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
+__global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(ApplyArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + kRingBytes);

@@ -54,15 +54,26 @@ constexpr int kTileThreads = 256;
 constexpr int kTileItems = 8;
 constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
 
-// Apply kernels.
-constexpr int kColTile = 1024;        // columns of one chunk item (128 consumers x 8)
-constexpr int kCombineCols = 512;     // columns of one combine task
+// Apply kernels.  Bulk copies reach full HBM bandwidth only from about 4 KB up, so an
+// item covers whole rows: a chunk over a column tile of up to 8192 columns (4096 for
+// an fp32 gradient), each grad row and the main_grad row one copy.
+constexpr int kMaxTileColsBf16 = 8192;
+constexpr int kMaxTileColsFp32 = 4096;
+constexpr int kCombineCols = 1024;    // columns of one combine task (4 KB partial rows)
 constexpr int kCombineBatch = 8;      // partial rows per combine ring item
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;           // 8 columns each per pass
 constexpr int kApplyThreads = kConsumers + 32;            // + one producer warp
-constexpr int kRingBytes = 96 * 1024;
+constexpr int kRingBytes = 200 * 1024;
 constexpr int kSlots = 16;
+
+// Column tile of the chunk items: the widest tile within the limit, split evenly.
+inline int tile_cols(int64_t hidden, bool grad_bf16) {
+  const int64_t lim = grad_bf16 ? kMaxTileColsBf16 : kMaxTileColsFp32;
+  const int64_t tiles = (hidden + lim - 1) / lim;
+  const int64_t per = (hidden + tiles - 1) / tiles;
+  return static_cast<int>((per + 7) / 8 * 8);
+}
 
 enum DeviceStatus { kStatusOk = 0, kStatusInvalid = 2, kStatusBadId = 4, kStatusTimeout = 5 };
 
@@ -172,6 +183,7 @@ struct ApplyArgs {
   long long mg_stride;     // elements
   int n;
   int hidden;
+  int tile_cols;           // columns of a chunk item (multiple of 8)
   long long num_embeddings;
   const Header* header;
   const int* tables;
