@@ -88,6 +88,9 @@ int check_sizes(int64_t n, int64_t V, int64_t H) {
   if (V < 1 || V > INT32_MAX) return fail(EWG_ERR_UNSUPPORTED, "num_embeddings outside [1, 2^31)");
   if (H < 8 || H > EWG_MAX_HIDDEN || H % 8 != 0)
     return fail(EWG_ERR_UNSUPPORTED, "hidden must be a multiple of 8 in [8, EWG_MAX_HIDDEN]");
+  // work items of the apply kernels are counted in 32 bits
+  if (n * ((H + ewg::kCombineCols - 1) / ewg::kCombineCols) >= (int64_t(1) << 31))
+    return fail(EWG_ERR_UNSUPPORTED, "num_tokens * ceil(hidden / 1024) must stay below 2^31");
   return EWG_OK;
 }
 
@@ -180,7 +183,8 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.mg_stride = mg_row_stride;
   a.n = static_cast<int>(n);
   a.hidden = static_cast<int>(H);
-  a.tile_cols = ewg::tile_cols(H, grad_dtype == EWG_BF16);
+  a.tile_cols_long = ewg::tile_cols(H, grad_dtype == EWG_BF16, true);
+  a.tile_cols_rest = ewg::tile_cols(H, grad_dtype == EWG_BF16, false);
   a.num_embeddings = V;
   a.header = at<ewg::Header>(ws, L.header);
   a.tables = at<int>(ws, L.tables);

@@ -232,8 +232,9 @@ struct Producer {
   // One (chunk, column tile) item: the chunk's grad row segments, plus the main_grad
   // segment when the run has no other chunk.
   __device__ bool chunk_item(const Desc& d, int tile) {
-    const int col0 = tile * a.tile_cols;
-    const int cols = min(a.tile_cols, a.hidden - col0);
+    const int tc = LONG ? a.tile_cols_long : a.tile_cols_rest;
+    const int col0 = tile * tc;
+    const int cols = min(tc, a.hidden - col0);
     const int meta = d.w[2].w;
     const int len = meta & 15;
     const int id = d.w[2].z;
@@ -320,53 +321,55 @@ template <bool GBF16, bool MBF16, bool LONG>
 __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   Producer<GBF16, MBF16, LONG> P(a, s, ring);
   const int parts = s.num_parts;
-  const int T = (a.hidden + a.tile_cols - 1) / a.tile_cols;
-  const long long G = gridDim.x;
-  long long idx = blockIdx.x;
-
-  if (!LONG) {   // combine tasks first
-    const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
-    const long long n_tasks = static_cast<long long>(s.prefix[2][parts]) * Tc;
-    int cur = 0;
-    for (; idx < n_tasks && P.ok; idx += G) {
-      const int r = static_cast<int>(idx / Tc);
-      const int group = static_cast<int>(idx - static_cast<long long>(r) * Tc);
-      const int ri = list_index(s.prefix[2], s.offset[2], parts, r, cur);
-      const int4 run = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
-      P.ok = P.combine_task(run, group);
-    }
-    idx -= n_tasks;   // now an ordinal into the chunk items
-  }
-
+  const int tc = LONG ? a.tile_cols_long : a.tile_cols_rest;
+  const int T = (a.hidden + tc - 1) / tc;
+  const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
+  // Work items, in the order they are handed out: the combine tasks (apply_rest only)
+  // and then the chunk items.  Counts fit in 32 bits (checked on the host).
+  const int n_tasks = LONG ? 0 : s.prefix[2][parts] * Tc;
   const int list = LONG ? 0 : 1;
-  const long long n_items = static_cast<long long>(s.prefix[list][parts]) * T;
-  int cur = 0;
-  // A ring of kAhead descriptors loaded kAhead items ahead.  The loop over the ring is
-  // unrolled so that every slot keeps its own registers: copying a register whose load
-  // is still in flight would stall the producer on that load.
-  constexpr int kAhead = 4;
-  Desc d[kAhead];
-  long long o[kAhead];
+  const int total = n_tasks + s.prefix[list][parts] * T;
+  int* work = const_cast<int*>(&a.header->work[LONG ? 0 : 1]);
+  int cur_run = 0, cur_chunk = 0;
+
+  // The entry an item needs: its long-run table row (combine) or chunk descriptor.
+  auto fetch = [&](int item) {
+    Desc d{};
+    if (item < n_tasks) {
+      const int ri = list_index(s.prefix[2], s.offset[2], parts, item / Tc, cur_run);
+      d.w[0] = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
+    } else if (item < total) {
+      const int o = item - n_tasks;
+      d = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts, o / T, cur_chunk));
+    }
+    return d;
+  };
+  auto run_item = [&](int item, const Desc& d) {
+    if (item < n_tasks) return P.combine_task(d.w[0], item % Tc);
+    return P.chunk_item(d, (item - n_tasks) % T);
+  };
+
+  // Items are claimed one at a time from the kernel's counter (a CTA's claims increase).
+  // Step k processes the item claimed at step k-3, whose entry was fetched at step k-2,
+  // fetches the entry of the item claimed at step k-1 and claims a new one.  The three
+  // slots are unrolled so each keeps its own registers.
+  int it[3];
+  Desc d[3];
 #pragma unroll
-  for (int j = 0; j < kAhead; ++j) {
-    o[j] = idx + j * G;
-    if (o[j] < n_items)
-      d[j] = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
-                                            static_cast<int>(o[j] / T), cur));
-  }
-  bool more = o[0] < n_items;
-  while (more && P.ok) {
+  for (int j = 0; j < 3; ++j) it[j] = atomicAdd(work, 1);
+  d[0] = fetch(it[0]);
+  d[1] = fetch(it[1]);
+  bool more = true;
+  while (more) {
 #pragma unroll
-    for (int j = 0; j < kAhead; ++j) {
-      if (more && P.ok) {
-        if (o[j] >= n_items) {
+    for (int j = 0; j < 3; ++j) {
+      if (more) {
+        d[(j + 2) % 3] = fetch(it[(j + 2) % 3]);
+        if (it[j] >= total || !P.ok) {
           more = false;
         } else {
-          P.ok = P.chunk_item(d[j], static_cast<int>(o[j] % T));
-          o[j] += kAhead * G;
-          if (o[j] < n_items)
-            d[j] = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts,
-                                                  static_cast<int>(o[j] / T), cur));
+          P.ok = run_item(it[j], d[j]);
+          it[j] = atomicAdd(work, 1);
         }
       }
     }
@@ -487,6 +490,17 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(ApplyArgs a) {
     return;
   }
   consume<GBF16, MBF16>(a, s, ring);
+  // The last CTA to finish re-arms the kernel's work counter, so that one plan can
+  // serve further ewg_apply calls.  Every CTA claims its last item before its
+  // consumers see the end of its stream, so no claim can follow this reset.
+  if (t == 0) {
+    Header* hw = const_cast<Header*>(h);
+    const int k = LONG ? 0 : 1;
+    if (atomicAdd(&hw->done[k], 1) == static_cast<int>(gridDim.x) - 1) {
+      hw->work[k] = 0;
+      hw->done[k] = 0;
+    }
+  }
 }
 
 constexpr size_t kApplySmem = kRingBytes + sizeof(Smem);

@@ -67,9 +67,14 @@ constexpr int kApplyThreads = kConsumers + 32;            // + one producer warp
 constexpr int kRingBytes = 200 * 1024;
 constexpr int kSlots = 16;
 
+// Long-run chunks carry 10 rows, so their items use tiles of at most 4096 columns:
+// twice as many, half-size items keep the end of apply_long short.
+constexpr int kMaxLongTileCols = 4096;
+
 // Column tile of the chunk items: the widest tile within the limit, split evenly.
-inline int tile_cols(int64_t hidden, bool grad_bf16) {
-  const int64_t lim = grad_bf16 ? kMaxTileColsBf16 : kMaxTileColsFp32;
+inline int tile_cols(int64_t hidden, bool grad_bf16, bool long_chunks) {
+  int64_t lim = grad_bf16 ? kMaxTileColsBf16 : kMaxTileColsFp32;
+  if (long_chunks && lim > kMaxLongTileCols) lim = kMaxLongTileCols;
   const int64_t tiles = (hidden + lim - 1) / lim;
   const int64_t per = (hidden + tiles - 1) / tiles;
   return static_cast<int>((per + 7) / 8 * 8);
@@ -84,7 +89,9 @@ struct Header {
   int num_parts;
   long long num_embeddings;
   int bad_ids;
-  int pad[57];
+  int work[2];           // next item of apply_long / apply_rest (zeroed by the plan)
+  int done[2];           // CTAs of apply_long / apply_rest that have finished
+  int pad[53];
 };
 static_assert(sizeof(Header) == 256, "header is one 256-byte region");
 
@@ -183,7 +190,8 @@ struct ApplyArgs {
   long long mg_stride;     // elements
   int n;
   int hidden;
-  int tile_cols;           // columns of a chunk item (multiple of 8)
+  int tile_cols_long;      // columns of a long-run chunk item (multiple of 8)
+  int tile_cols_rest;      // columns of a short-run chunk item (multiple of 8)
   long long num_embeddings;
   const Header* header;
   const int* tables;

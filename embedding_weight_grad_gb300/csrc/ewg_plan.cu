@@ -268,6 +268,8 @@ __device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
   h->num_embeddings = a.num_embeddings;
   h->num_parts = num_parts;
   h->bad_ids = bad;
+  h->work[0] = h->work[1] = 0;
+  h->done[0] = h->done[1] = 0;
   h->status = bad ? EWG_ERR_ID_OUT_OF_RANGE : EWG_OK;
 }
 
