@@ -90,7 +90,7 @@ int check_sizes(int64_t n, int64_t V, int64_t H) {
     return fail(EWG_ERR_UNSUPPORTED, "hidden must be a multiple of 8 in [8, EWG_MAX_HIDDEN]");
   // work items of the apply kernels are counted in 32 bits
   if (n * ((H + ewg::kCombineCols - 1) / ewg::kCombineCols) >= (int64_t(1) << 31))
-    return fail(EWG_ERR_UNSUPPORTED, "num_tokens * ceil(hidden / 1024) must stay below 2^31");
+    return fail(EWG_ERR_UNSUPPORTED, "num_tokens * ceil(hidden / 512) must stay below 2^31");
   return EWG_OK;
 }
 

@@ -324,39 +324,46 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int tc = LONG ? a.tile_cols_long : a.tile_cols_rest;
   const int T = (a.hidden + tc - 1) / tc;
   const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
-  // Work items, in the order they are handed out: the combine tasks (apply_rest only)
-  // and then the chunk items.  Counts fit in 32 bits (checked on the host).
-  const int n_tasks = LONG ? 0 : s.prefix[2][parts] * Tc;
+  // Work items, in the order they are handed out: the chunk items, then (apply_rest
+  // only) the combine tasks.  Counts fit in 32 bits (checked on the host).
   const int list = LONG ? 0 : 1;
-  const int total = n_tasks + s.prefix[list][parts] * T;
+  const int n_chunk_items = s.prefix[list][parts] * T;
+  const int total = n_chunk_items + (LONG ? 0 : s.prefix[2][parts] * Tc);
   int* work = const_cast<int*>(&a.header->work[LONG ? 0 : 1]);
+  const int G = static_cast<int>(gridDim.x);
   int cur_run = 0, cur_chunk = 0;
+  bool waited = LONG;   // apply_rest waits for apply_long before its first combine task
 
-  // The entry an item needs: its long-run table row (combine) or chunk descriptor.
+  // The entry an item needs: its chunk descriptor or its long-run table row.
   auto fetch = [&](int item) {
     Desc d{};
-    if (item < n_tasks) {
-      const int ri = list_index(s.prefix[2], s.offset[2], parts, item / Tc, cur_run);
-      d.w[0] = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
+    if (item < n_chunk_items) {
+      d = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts, item / T, cur_chunk));
     } else if (item < total) {
-      const int o = item - n_tasks;
-      d = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts, o / T, cur_chunk));
+      const int ri = list_index(s.prefix[2], s.offset[2], parts, (item - n_chunk_items) / Tc, cur_run);
+      d.w[0] = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
     }
     return d;
   };
   auto run_item = [&](int item, const Desc& d) {
-    if (item < n_tasks) return P.combine_task(d.w[0], item % Tc);
-    return P.chunk_item(d, (item - n_tasks) % T);
+    if (item < n_chunk_items) return P.chunk_item(d, item % T);
+    if (!waited) {   // the partial rows are apply_long's output
+      ptx::pdl_wait_prior_grid();
+      waited = true;
+    }
+    return P.combine_task(d.w[0], (item - n_chunk_items) % Tc);
   };
+  // Claims: item blockIdx.x first, then G + the kernel's counter, one at a time (a CTA's
+  // claims increase).  Step k processes the item claimed at step k-3, whose entry was
+  // fetched at step k-2, fetches the entry of the item claimed at step k-1 and claims
+  // a new one.  The three slots are unrolled so each keeps its own registers.
+  auto claim = [&]() { return G + atomicAdd(work, 1); };
 
-  // Items are claimed one at a time from the kernel's counter (a CTA's claims increase).
-  // Step k processes the item claimed at step k-3, whose entry was fetched at step k-2,
-  // fetches the entry of the item claimed at step k-1 and claims a new one.  The three
-  // slots are unrolled so each keeps its own registers.
   int it[3];
   Desc d[3];
-#pragma unroll
-  for (int j = 0; j < 3; ++j) it[j] = atomicAdd(work, 1);
+  it[0] = blockIdx.x;
+  it[1] = claim();
+  it[2] = claim();
   d[0] = fetch(it[0]);
   d[1] = fetch(it[1]);
   bool more = true;
@@ -369,12 +376,14 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
           more = false;
         } else {
           P.ok = run_item(it[j], d[j]);
-          it[j] = atomicAdd(work, 1);
+          it[j] = claim();
         }
       }
     }
   }
   P.finish_stream();
+  // every CTA waits, so this grid never completes before the previous one
+  if (!waited) ptx::pdl_wait_prior_grid();
 }
 
 template <bool GBF16, bool MBF16>
@@ -446,9 +455,14 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(ApplyArgs a) {
     ptx::fence_mbar_init();
     s.abort = 0;
   }
-  // every CTA waits for the previous kernel, so this grid never completes before it
-  ptx::pdl_wait_prior_grid();
-  if (LONG) ptx::pdl_launch_dependents();
+  // apply_long waits for the plan.  apply_rest is launched only once every apply_long
+  // CTA has passed that wait, so the plan is complete and visible to it; it waits for
+  // apply_long itself only before reading partial rows (and, like every CTA of both
+  // kernels, before it exits, so neither grid completes before its predecessor).
+  if (LONG) {
+    ptx::pdl_wait_prior_grid();
+    ptx::pdl_launch_dependents();
+  }
 
   const Header* h = a.header;
   if (t == 0) {   // one reader decides for the whole CTA
@@ -460,7 +474,10 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(ApplyArgs a) {
     s.num_parts = go ? h->num_parts : -1;
   }
   __syncthreads();
-  if (s.num_parts < 0) return;
+  if (s.num_parts < 0) {
+    if (!LONG) ptx::pdl_wait_prior_grid();
+    return;
+  }
   if (t < 32) {   // partition tables -> per-list prefix counts
     const int parts = s.num_parts;
     for (int list = 0; list < 3; ++list) {

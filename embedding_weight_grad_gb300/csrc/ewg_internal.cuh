@@ -59,7 +59,8 @@ constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
 // an fp32 gradient), each grad row and the main_grad row one copy.
 constexpr int kMaxTileColsBf16 = 8192;
 constexpr int kMaxTileColsFp32 = 4096;
-constexpr int kCombineCols = 1024;    // columns of one combine task (4 KB partial rows)
+constexpr int kCombineCols = 512;     // columns of one combine task (2 KB partial rows; they
+                                      // run last, so they are kept small)
 constexpr int kCombineBatch = 8;      // partial rows per combine ring item
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;           // 8 columns each per pass

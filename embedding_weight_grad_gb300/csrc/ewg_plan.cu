@@ -300,7 +300,8 @@ __device__ void smem_radix_sort(uint32_t*& ks, uint32_t*& vs, uint32_t*& kd, uin
     const int sh = pass * a.digit_bits;
     const int bits = min(a.digit_bits, a.id_bits - sh);
     const uint32_t B = 1u << bits, mask = B - 1;
-    for (uint32_t i = t; i < NW * B; i += NT) cnt[(i / B) * kStride + (i % B)] = 0;
+    for (int w = 0; w < NW; ++w)
+      for (uint32_t d = t; d < B; d += NT) cnt[w * kStride + d] = 0;
     __syncthreads();
     uint32_t rank[MAXR], dig[MAXR];
 #pragma unroll
@@ -354,6 +355,29 @@ __device__ void smem_radix_sort(uint32_t*& ks, uint32_t*& vs, uint32_t*& kd, uin
 __device__ __forceinline__ int hash_part(uint32_t id) {
   static_assert(kHashParts == 64, "hash uses the top 6 bits");
   return static_cast<int>((id * 0x9E3779B1u) >> 26);
+}
+
+// Lists the m sorted pairs of hash partition `part` and writes its lists, tables and
+// (partition 0) the header.  S_b: tokens of the partitions before this one.
+template <int NT, int ITEMS>
+__device__ void list_partition(const PlanArgs& a, const uint32_t* ks, const uint32_t* vs, int m,
+                               int S_b, int part, int* swi, long long* sw64) {
+  Listing<NT, ITEMS> L;
+  L.compute(ks, m, 0, 0, m - 1, swi);
+  long long tot = 0;
+  const long long prefix =
+      block_exclusive_scan<NT, long long>(L.counts(m, 0), SumOp(), 0ll, sw64, &tot);
+  const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
+  EmitBases eb;
+  eb.long_desc = S_b;
+  eb.short_desc = S_b + n_long;
+  eb.partial = (2 * S_b) / 11 + part;
+  eb.run = S_b / 11 + part;
+  L.emit(a, vs, m, 0, prefix, eb);
+  if (threadIdx.x == 0) {
+    write_tables(a, part, n_long, eb.long_desc, n_short, eb.short_desc, n_runs, eb.run);
+    if (part == 0) write_header(a, kHashParts, 0);
+  }
 }
 
 constexpr int kHashWarps = kHashThreads / 32;
@@ -434,23 +458,13 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   __syncthreads();
   const int m = total;
 
-  // 3. sort by id, 4. list runs and chunks
+  // 3. sort by id, 4. list runs and chunks (fewer slots per thread for small
+  // partitions: blocked shared-memory reads conflict in proportion to the slots)
   smem_radix_sort<kHashThreads, kHashItems>(ks, vs, kd, vd, m, a, cnt, sw64);
-  Listing<kHashThreads, kHashItems> L;
-  L.compute(ks, m, 0, 0, m - 1, swi);
-  long long tot = 0;
-  const long long prefix =
-      block_exclusive_scan<kHashThreads, long long>(L.counts(m, 0), SumOp(), 0ll, sw64, &tot);
-  const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
-  EmitBases eb;
-  eb.long_desc = S_b;
-  eb.short_desc = S_b + n_long;
-  eb.partial = (2 * S_b) / 11 + part;
-  eb.run = S_b / 11 + part;
-  L.emit(a, vs, m, 0, prefix, eb);
-  if (t == 0) {
-    write_tables(a, part, n_long, eb.long_desc, n_short, eb.short_desc, n_runs, eb.run);
-    if (part == 0) write_header(a, kHashParts, 0);
+  if (m <= kHashThreads * 4) {
+    list_partition<kHashThreads, 4>(a, ks, vs, m, S_b, part, swi, sw64);
+  } else {
+    list_partition<kHashThreads, kHashItems>(a, ks, vs, m, S_b, part, swi, sw64);
   }
 }
 
@@ -541,7 +555,8 @@ __global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const
   const int sh = pass * a.digit_bits;
   const uint32_t B = 1u << min(a.digit_bits, a.id_bits - sh), mask = B - 1;
   const uint32_t lt = (1u << lane) - 1u;
-  for (uint32_t i = t; i < NW * B; i += kTileThreads) cnt[(i / B) * kStride + (i % B)] = 0;
+  for (int w = 0; w < NW; ++w)
+    for (uint32_t d = t; d < B; d += kTileThreads) cnt[w * kStride + d] = 0;
   __syncthreads();
   uint32_t rank[kTileItems], dig[kTileItems];
 #pragma unroll
