@@ -174,11 +174,9 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t H, voi
 
 int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg, int mg_dtype,
              int64_t n, int64_t V, int64_t H, int64_t mg_row_stride, void* ws, int num_sms,
-             cudaStream_t stream, const void* ids, int ids_dtype) {
+             cudaStream_t stream) {
   const ewg::Layout L = ewg::make_layout(n, H);
   ewg::ApplyArgs a{};
-  a.ids = ids;   // NULL: no main_grad prefetch
-  a.ids_int64 = ids_dtype == EWG_INT64;
   a.grad = grad;
   a.grad_stride = grad_row_stride;
   a.main_grad = mg;
@@ -235,8 +233,7 @@ int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const voi
   rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, s);
   if (rc) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
-                  num_embeddings, hidden, main_grad_row_stride, workspace, sms, s, ids,
-                  ids_dtype);
+                  num_embeddings, hidden, main_grad_row_stride, workspace, sms, s);
 }
 
 int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_embeddings,
@@ -269,7 +266,7 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* m
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
                   num_embeddings, hidden, main_grad_row_stride, workspace, sms,
-                  static_cast<cudaStream_t>(stream), nullptr, EWG_INT64);
+                  static_cast<cudaStream_t>(stream));
 }
 
 int ewg_read_status(const void* workspace, void* stream, int* status) {
