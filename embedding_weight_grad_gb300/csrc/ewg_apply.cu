@@ -460,19 +460,6 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(ApplyArgs a) {
   // apply_long itself only before reading partial rows (and, like every CTA of both
   // kernels, before it exits, so neither grid completes before its predecessor).
   if (LONG) {
-    // While the plan still runs, the HBM is nearly idle: pull the first rows of grad
-    // into L2 (every grad row is read exactly once later).  These CTAs launch early on
-    // the SMs the plan leaves free; the rows need nothing from the plan.
-    if (t == kConsumers) {
-      const int rows = static_cast<int>(static_cast<long long>(a.n) * kPrefetchNum / kPrefetchDen);
-      const int r0 = static_cast<int>(static_cast<long long>(rows) * blockIdx.x / gridDim.x);
-      const int r1 = static_cast<int>(static_cast<long long>(rows) * (blockIdx.x + 1) / gridDim.x);
-      const long long gsz = GBF16 ? 2 : 4;
-      const char* g = static_cast<const char*>(a.grad);
-      for (int r = r0; r < r1; ++r)
-        ptx::bulk_prefetch_l2(g + static_cast<long long>(r) * a.grad_stride * gsz,
-                              static_cast<uint32_t>(a.hidden * gsz));
-    }
     ptx::pdl_wait_prior_grid();
     ptx::pdl_launch_dependents();
   }

@@ -68,10 +68,6 @@ constexpr int kApplyThreads = kConsumers + 32;            // + one producer warp
 constexpr int kRingBytes = 200 * 1024;
 constexpr int kSlots = 16;
 
-// Fraction of the grad rows that apply_long prefetches into L2 while the plan runs.
-constexpr int kPrefetchNum = 1;
-constexpr int kPrefetchDen = 2;
-
 // Long-run chunks carry 10 rows, so their items use tiles of at most 4096 columns:
 // twice as many, half-size items keep the end of apply_long short.
 constexpr int kMaxLongTileCols = 4096;

@@ -5,18 +5,18 @@
 // give every sorted slot its run, list the chunks of at most NROWS slots and the runs
 // longer than NROWS.
 //
-// Sorting is an LSD radix sort over the id bits only.  Keys arrive in position order
-// and every pass is stable, so positions stay ascending inside each run without passes
-// of their own.
-//
 // Up to 8192 tokens (hashed path): 64 CTAs each read all ids and keep the ids of one
-// hash partition (id * golden-ratio constant, top 6 bits), in position order; each
-// CTA then sorts and lists its partition alone in shared memory.  A run never spans
-// two partitions, so no CTA waits for another, and the apply kernels find each
-// partition's lists through the partition tables.
+// hash partition (id * golden-ratio constant, top 6 bits), in position order.  Each
+// CTA groups its partition through a shared-memory hash table and ranks every key
+// among the earlier keys of its id; a key's chunk and place in the chunk follow from
+// its rank, so the pairs are never sorted.  A run never spans two partitions, so no
+// CTA waits for another, and the apply kernels find each partition's lists through
+// the partition tables.
 //
-// Above 8192 tokens (multi-tile path): histogram / scan / scatter kernels over tiles
-// of 2048 keys per radix pass, then count / scan / emit kernels for the listing.
+// Above 8192 tokens (multi-tile path): an LSD radix sort over the id bits only (keys
+// arrive in position order and every pass is stable, so positions stay ascending in
+// each run without passes of their own) as histogram / scan / scatter kernels over
+// tiles of 2048 keys, then count / scan / emit kernels for the listing.
 //
 // The listing gives every sorted slot s its run's first slot rs and last slot re.
 // Slot s starts a chunk when (s - rs) % NROWS == 0.
@@ -283,118 +283,43 @@ __device__ void write_tables(const PlanArgs& a, int part, int long_cnt, int long
   a.tables[kRunOff * kMaxParts + part] = run_off;
 }
 
-// Stable LSD radix sort of m (key, value) pairs in shared memory by the id bits.  Warp w
-// ranks the contiguous key range [w*K, (w+1)*K) in (round, lane) order; counters are laid
-// out [warp][bucket] so that the lanes of one warp hit distinct banks.
-template <int NT, int MAXR>
-__device__ void smem_radix_sort(uint32_t*& ks, uint32_t*& vs, uint32_t*& kd, uint32_t*& vd, int m,
-                                const PlanArgs& a, uint32_t* cnt, long long* sw64) {
-  constexpr int NW = NT / 32;
-  constexpr int kStride = 1 << kMaxDigitBits;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const int K = ((m + NW - 1) / NW + 31) / 32 * 32;
-  const int rounds = K / 32;
-  const int w0 = warp * K;
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int pass = 0; pass < a.passes; ++pass) {
-    const int sh = pass * a.digit_bits;
-    const int bits = min(a.digit_bits, a.id_bits - sh);
-    const uint32_t B = 1u << bits, mask = B - 1;
-    for (int w = 0; w < NW; ++w)
-      for (uint32_t d = t; d < B; d += NT) cnt[w * kStride + d] = 0;
-    __syncthreads();
-    uint32_t rank[MAXR], dig[MAXR];
-#pragma unroll
-    for (int r = 0; r < MAXR; ++r) {
-      rank[r] = 0;
-      dig[r] = 0;
-      if (r < rounds) {
-        const int idx = w0 + r * 32 + lane;
-        const bool valid = idx < m;
-        const uint32_t d = valid ? (ks[idx] >> sh) & mask : 0xffffffffu;
-        const unsigned peers = __match_any_sync(kFull, d);
-        uint32_t prior = 0;
-        if (valid) prior = cnt[warp * kStride + d];
-        __syncwarp();
-        if (valid && lane == 31 - __clz(peers)) cnt[warp * kStride + d] = prior + __popc(peers);
-        __syncwarp();
-        rank[r] = prior + __popc(peers & lt);
-        dig[r] = d;
-      }
-    }
-    __syncthreads();
-    uint32_t tot = 0;
-    if (t < static_cast<int>(B))
-      for (int w = 0; w < NW; ++w) tot += cnt[w * kStride + t];
-    long long run = block_exclusive_scan<NT, long long>(tot, SumOp(), 0ll, sw64, nullptr);
-    if (t < static_cast<int>(B)) {
-      for (int w = 0; w < NW; ++w) {
-        const uint32_t c = cnt[w * kStride + t];
-        cnt[w * kStride + t] = static_cast<uint32_t>(run);
-        run += c;
-      }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < MAXR; ++r) {
-      if (r < rounds) {
-        const int idx = w0 + r * 32 + lane;
-        if (idx < m) {
-          const uint32_t dst = cnt[warp * kStride + dig[r]] + rank[r];
-          kd[dst] = ks[idx];
-          vd[dst] = vs[idx];
-        }
-      }
-    }
-    __syncthreads();
-    uint32_t* tk = ks; ks = kd; kd = tk;
-    uint32_t* tv = vs; vs = vd; vd = tv;
-  }
-}
-
 __device__ __forceinline__ int hash_part(uint32_t id) {
   static_assert(kHashParts == 64, "hash uses the top 6 bits");
   return static_cast<int>((id * 0x9E3779B1u) >> 26);
 }
 
-// Lists the m sorted pairs of hash partition `part` and writes its lists, tables and
-// (partition 0) the header.  S_b: tokens of the partitions before this one.
-template <int NT, int ITEMS>
-__device__ void list_partition(const PlanArgs& a, const uint32_t* ks, const uint32_t* vs, int m,
-                               int S_b, int part, int* swi, long long* sw64) {
-  Listing<NT, ITEMS> L;
-  L.compute(ks, m, 0, 0, m - 1, swi);
-  long long tot = 0;
-  const long long prefix =
-      block_exclusive_scan<NT, long long>(L.counts(m, 0), SumOp(), 0ll, sw64, &tot);
-  const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
-  EmitBases eb;
-  eb.long_desc = S_b;
-  eb.short_desc = S_b + n_long;
-  eb.partial = (2 * S_b) / 11 + part;
-  eb.run = S_b / 11 + part;
-  L.emit(a, vs, m, 0, prefix, eb);
-  if (threadIdx.x == 0) {
-    write_tables(a, part, n_long, eb.long_desc, n_short, eb.short_desc, n_runs, eb.run);
-    if (part == 0) write_header(a, kHashParts, 0);
-  }
+// Slot hash of the per-partition table, independent of the partition hash.
+__device__ __forceinline__ uint32_t hash_slot(uint32_t id, int tbits) {
+  return (id * 0x85EBCA77u) >> (32 - tbits);
 }
 
 constexpr int kHashWarps = kHashThreads / 32;
-constexpr size_t kHashSmem = static_cast<size_t>(4) * kHashMaxN * 4 +
-                             static_cast<size_t>(kHashWarps) * (1 << kMaxDigitBits) * 4;
+constexpr int kTableMax = kHashMaxN;           // table slots at most (a power of two)
+constexpr uint32_t kEmptySlot = 0xffffffffu;
+constexpr int kRankShift = 13;                 // key info word: slot | rank << 13
+static_assert(kTableMax <= (1 << kRankShift) && kHashMaxN <= (1 << (32 - kRankShift)),
+              "slot and rank must pack into one word");
+constexpr size_t kHashSmem =
+    static_cast<size_t>(2) * kHashMaxN * 4 + static_cast<size_t>(3) * kTableMax * 4;
 
 // ---------------------------------------------------------------------------
-// Hashed plan: CTA b handles the ids whose hash partition is b.
+// Hashed plan: CTA `part` handles the ids whose hash partition is `part`.
+//
+// Inside the partition a shared-memory hash table gives every distinct id a slot.  One
+// warp then walks the keys in position order, 32 at a time, and gives each key its
+// rank among the earlier keys of its id (match.any groups equal slots within the 32).
+// A key's chunk is rank / NROWS and its place in the chunk is rank % NROWS, so the
+// (token, position) pairs never need to be sorted: after a scan over the table assigns
+// every run its descriptors, every key writes its own position word.
 
 __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a) {
   ptx::pdl_launch_dependents();
   extern __shared__ __align__(16) uint32_t sm[];
-  uint32_t* ks = sm;
-  uint32_t* vs = ks + kHashMaxN;
-  uint32_t* kd = vs + kHashMaxN;
-  uint32_t* vd = kd + kHashMaxN;
-  uint32_t* cnt = vd + kHashMaxN;
+  uint32_t* kpos = sm;                   // position of key i (keys in position order)
+  uint32_t* kinfo = kpos + kHashMaxN;    // id of key i; then slot | rank << kRankShift
+  uint32_t* tkey = kinfo + kHashMaxN;    // table: id of the slot
+  uint32_t* tcnt = tkey + kTableMax;     // table: occurrences of the id (run length)
+  uint32_t* tbase = tcnt + kTableMax;    // table: descriptor of the run's first chunk
   __shared__ int wc[kHashItems * kHashWarps];
   __shared__ long long sw64[kHashWarps];
   __shared__ int swi[kHashWarps];
@@ -439,32 +364,120 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
     return;
   }
 
-  // 2. this partition's (id, position) pairs, compacted in position order
-  int total = 0;
+  // 2. this partition's keys, compacted in position order
+  int m = 0;
   {
     const int v = t < kHashItems * kHashWarps ? wc[t] : 0;
-    const int off = block_exclusive_scan<kHashThreads, int>(v, SumIntOp(), 0, swi, &total);
+    const int off = block_exclusive_scan<kHashThreads, int>(v, SumIntOp(), 0, swi, &m);
     if (t < kHashItems * kHashWarps) wc[t] = off;
     __syncthreads();
   }
 #pragma unroll
   for (int r = 0; r < kHashItems; ++r) {
     if ((ballot[r] >> lane) & 1u) {
-      const int slot = wc[r * kHashWarps + warp] + __popc(ballot[r] & lt);
-      ks[slot] = key[r];
-      vs[slot] = static_cast<uint32_t>(r * kHashThreads + t);
+      const int i = wc[r * kHashWarps + warp] + __popc(ballot[r] & lt);
+      kpos[i] = static_cast<uint32_t>(r * kHashThreads + t);
+      kinfo[i] = key[r];
+    }
+  }
+  int tbits = 5;   // table of at least 2m slots (at least m, kTableMax >= every m)
+  while ((1 << tbits) < 2 * m && (1 << tbits) < kTableMax) ++tbits;
+  const int TS = 1 << tbits;
+  for (int s = t; s < TS; s += kHashThreads) {
+    tkey[s] = kEmptySlot;
+    tcnt[s] = 0;
+  }
+  __syncthreads();
+
+  // 3. the slot of every key: linear probing; there are at least as many slots as ids,
+  // so every probe sequence ends within TS steps
+  for (int i = t; i < m; i += kHashThreads) {
+    const uint32_t id = kinfo[i];
+    uint32_t h = hash_slot(id, tbits);
+    for (int probe = 0; probe < TS; ++probe) {
+      const uint32_t old = atomicCAS(&tkey[h], kEmptySlot, id);
+      if (old == kEmptySlot || old == id) break;
+      h = (h + 1) & static_cast<uint32_t>(TS - 1);
+    }
+    kinfo[i] = h;
+  }
+  __syncthreads();
+
+  // 4. ranks in position order, one warp, 32 keys per step
+  if (warp == 0) {
+    for (int i0 = 0; i0 < m; i0 += 32) {
+      const int i = i0 + lane;
+      const bool valid = i < m;
+      const uint32_t s = valid ? kinfo[i] : kEmptySlot;
+      const unsigned peers = __match_any_sync(kFull, s);
+      uint32_t prior = 0;
+      if (valid) prior = tcnt[s];
+      __syncwarp();
+      if (valid && lane == 31 - __clz(peers)) tcnt[s] = prior + __popc(peers);
+      __syncwarp();
+      if (valid) kinfo[i] = s | ((prior + __popc(peers & lt)) << kRankShift);
     }
   }
   __syncthreads();
-  const int m = total;
 
-  // 3. sort by id, 4. list runs and chunks (fewer slots per thread for small
-  // partitions: blocked shared-memory reads conflict in proportion to the slots)
-  smem_radix_sort<kHashThreads, kHashItems>(ks, vs, kd, vd, m, a, cnt, sw64);
-  if (m <= kHashThreads * 4) {
-    list_partition<kHashThreads, 4>(a, ks, vs, m, S_b, part, swi, sw64);
-  } else {
-    list_partition<kHashThreads, kHashItems>(a, ks, vs, m, S_b, part, swi, sw64);
+  // 5. runs: a scan over the table gives each run its first descriptor; long runs also
+  // get their partial rows and their row of the long-run table
+  long long cnt = 0;
+  for (int s = t; s < TS; s += kHashThreads) {
+    const int L = static_cast<int>(tcnt[s]);
+    if (L > kNrows) {
+      cnt += (static_cast<long long>((L + kNrows - 1) / kNrows) << kField) + 1;
+    } else if (L > 0) {
+      cnt += 1ll << (2 * kField);
+    }
+  }
+  long long tot = 0;
+  const long long pre = block_exclusive_scan<kHashThreads, long long>(cnt, SumOp(), 0ll, sw64, &tot);
+  const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
+  const int long_desc = S_b, short_desc = S_b + n_long;
+  const int partial_base = (2 * S_b) / 11 + part, run_base = S_b / 11 + part;
+  {
+    int li = field_long(pre), si = field_short(pre), ri = field_runs(pre);
+    for (int s = t; s < TS; s += kHashThreads) {
+      const int L = static_cast<int>(tcnt[s]);
+      if (L > kNrows) {
+        const int C = (L + kNrows - 1) / kNrows;
+        tbase[s] = static_cast<uint32_t>(long_desc + li);
+        reinterpret_cast<int4*>(a.runs)[run_base + ri] =
+            make_int4(partial_base + li, C, static_cast<int>(tkey[s]), 0);
+        li += C;
+        ++ri;
+      } else if (L > 0) {
+        tbase[s] = static_cast<uint32_t>(short_desc + si);
+        ++si;
+      }
+    }
+  }
+  __syncthreads();
+
+  // 6. every key writes its position into its chunk; the first key of a chunk also
+  // writes the chunk's id, length, index in the run, partial row and the run's size
+  for (int i = t; i < m; i += kHashThreads) {
+    const uint32_t info = kinfo[i];
+    const int s = static_cast<int>(info & ((1u << kRankShift) - 1u));
+    const int r = static_cast<int>(info >> kRankShift);
+    const int L = static_cast<int>(tcnt[s]);
+    const int c = r / kNrows, k = r - c * kNrows;
+    const int desc = static_cast<int>(tbase[s]) + c;
+    int* d = a.chunks + static_cast<long long>(desc) * kChunkWords;
+    d[kDescPos + k] = static_cast<int>(kpos[i]);
+    if (k == 0) {
+      const bool is_long = L > kNrows;
+      const int len = min(kNrows, L - r);
+      const int C = (L + kNrows - 1) / kNrows;
+      const int prow = is_long ? partial_base + (static_cast<int>(tbase[s]) - long_desc) + c : -1;
+      reinterpret_cast<int2*>(d)[kDescId / 2] = make_int2(static_cast<int>(tkey[s]), len | (c << 4));
+      reinterpret_cast<int4*>(d)[kDescPartial / 4] = make_int4(prow, C, 0, 0);
+    }
+  }
+  if (t == 0) {
+    write_tables(a, part, n_long, long_desc, n_short, short_desc, n_runs, run_base);
+    if (part == 0) write_header(a, kHashParts, 0);
   }
 }
 
