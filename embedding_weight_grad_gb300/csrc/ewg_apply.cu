@@ -325,33 +325,45 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int T = (a.hidden + tc - 1) / tc;
   const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
   // Work items, in the order they are handed out: the chunk items, then (apply_rest
-  // only) the combine tasks.  Counts fit in 32 bits (checked on the host).
+  // only) the combine tasks, which wait for apply_long.  Counts fit in 32 bits
+  // (checked on the host).
   const int list = LONG ? 0 : 1;
   const int n_chunk_items = s.prefix[list][parts] * T;
-  const int total = n_chunk_items + (LONG ? 0 : s.prefix[2][parts] * Tc);
+  const int n_tasks = LONG ? 0 : s.prefix[2][parts] * Tc;
+  const int first = n_chunk_items;
+  const int total = n_chunk_items + n_tasks;
   int* work = const_cast<int*>(&a.header->work[LONG ? 0 : 1]);
   const int G = static_cast<int>(gridDim.x);
   int cur_run = 0, cur_chunk = 0;
   bool waited = LONG;   // apply_rest waits for apply_long before its first combine task
 
   // The entry an item needs: its chunk descriptor or its long-run table row.
+  // chunk-item ordinal of an item, or -1 for a combine task
+  auto chunk_ord = [&](int item) {
+    if (item < first) return item;
+    if (item < first + n_tasks) return -1;
+    return item - n_tasks;
+  };
   auto fetch = [&](int item) {
     Desc d{};
-    if (item < n_chunk_items) {
-      d = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts, item / T, cur_chunk));
-    } else if (item < total) {
-      const int ri = list_index(s.prefix[2], s.offset[2], parts, (item - n_chunk_items) / Tc, cur_run);
+    if (item >= total) return d;
+    const int o = chunk_ord(item);
+    if (o >= 0) {
+      d = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts, o / T, cur_chunk));
+    } else {
+      const int ri = list_index(s.prefix[2], s.offset[2], parts, (item - first) / Tc, cur_run);
       d.w[0] = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
     }
     return d;
   };
   auto run_item = [&](int item, const Desc& d) {
-    if (item < n_chunk_items) return P.chunk_item(d, item % T);
+    const int o = chunk_ord(item);
+    if (o >= 0) return P.chunk_item(d, o % T);
     if (!waited) {   // the partial rows are apply_long's output
       ptx::pdl_wait_prior_grid();
       waited = true;
     }
-    return P.combine_task(d.w[0], (item - n_chunk_items) % Tc);
+    return P.combine_task(d.w[0], (item - first) % Tc);
   };
   // Claims: item blockIdx.x first, then G + the kernel's counter, one at a time (a CTA's
   // claims increase).  Step k processes the item claimed at step k-3, whose entry was
@@ -442,7 +454,7 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
 }
 
 template <bool GBF16, bool MBF16, bool LONG>
-__global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(ApplyArgs a) {
+__global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + kRingBytes);

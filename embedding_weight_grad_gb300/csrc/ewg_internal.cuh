@@ -57,15 +57,14 @@ constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
 // Apply kernels.  Bulk copies reach full HBM bandwidth only from about 4 KB up, so an
 // item covers whole rows: a chunk over a column tile of up to 8192 columns (4096 for
 // an fp32 gradient), each grad row and the main_grad row one copy.
-constexpr int kMaxTileColsBf16 = 8192;
-constexpr int kMaxTileColsFp32 = 4096;
-constexpr int kCombineCols = 512;     // columns of one combine task (2 KB partial rows; they
-                                      // run last, so they are kept small)
+constexpr int kMaxTileColsBf16 = 4096;
+constexpr int kMaxTileColsFp32 = 2048;
+constexpr int kCombineCols = 512;     // columns of one combine task (2 KB partial rows)
 constexpr int kCombineBatch = 8;      // partial rows per combine ring item
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;           // 8 columns each per pass
 constexpr int kApplyThreads = kConsumers + 32;            // + one producer warp
-constexpr int kRingBytes = 200 * 1024;
+constexpr int kRingBytes = 100 * 1024;
 constexpr int kSlots = 16;
 
 // Long-run chunks carry 10 rows, so their items use tiles of at most 4096 columns:

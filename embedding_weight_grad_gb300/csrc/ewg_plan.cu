@@ -390,16 +390,29 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   __syncthreads();
 
   // 3. the slot of every key: linear probing; there are at least as many slots as ids,
-  // so every probe sequence ends within TS steps
-  for (int i = t; i < m; i += kHashThreads) {
-    const uint32_t id = kinfo[i];
-    uint32_t h = hash_slot(id, tbits);
-    for (int probe = 0; probe < TS; ++probe) {
-      const uint32_t old = atomicCAS(&tkey[h], kEmptySlot, id);
-      if (old == kEmptySlot || old == id) break;
-      h = (h + 1) & static_cast<uint32_t>(TS - 1);
+  // so every probe sequence ends within TS steps.  Within a warp only one lane per
+  // distinct id probes (a hot id would otherwise serialise on one slot).
+  for (int i0 = warp * 32; i0 < m; i0 += kHashThreads) {
+    const int i = i0 + lane;
+    const bool valid = i < m;
+    const uint32_t id = valid ? kinfo[i] : kEmptySlot;
+    const unsigned peers = __match_any_sync(kFull, id);
+    const int leader = __ffs(peers) - 1;
+    uint32_t h = 0;
+    if (valid && lane == leader) {
+      h = hash_slot(id, tbits);
+      for (int probe = 0; probe < TS; ++probe) {
+        const uint32_t cur = tkey[h];
+        if (cur == id) break;
+        if (cur == kEmptySlot) {
+          const uint32_t old = atomicCAS(&tkey[h], kEmptySlot, id);
+          if (old == kEmptySlot || old == id) break;
+        }
+        h = (h + 1) & static_cast<uint32_t>(TS - 1);
+      }
     }
-    kinfo[i] = h;
+    h = __shfl_sync(kFull, h, leader);
+    if (valid) kinfo[i] = h;
   }
   __syncthreads();
 
