@@ -33,6 +33,13 @@ constexpr uint32_t kSpinLimit = 1u << 22;   // bounded mbarrier waits
 
 enum ItemKind { kEnd = -1, kShortChunk = 0, kLongChunk = 1, kCombine = 2 };
 
+// How the producer fills the ring: with one thread issuing cp.async.bulk (TMA) copies,
+// or with the whole producer warp issuing 16-byte cp.async copies (512 bytes per
+// instruction, completion tracked per lane on the slot's barrier).  Measured on the
+// large-vocabulary workload the bulk copies are faster, so they are the ones built.
+constexpr bool kWarpCopy = false;
+constexpr int kFullArrivals = kWarpCopy ? 33 : 1;   // 32 lanes + the info publisher
+
 struct Item {
   int off;        // byte offset of the item in the ring
   int rows;       // grad rows (chunks) or partial rows (combine) in the ring
@@ -182,13 +189,16 @@ struct Producer {
   uint32_t head = 0, tail = 0;
   uint64_t pol_stream;
   bool ok = true;
+  const uint32_t lane = threadIdx.x & 31;
 
   __device__ Producer(const ApplyArgs& args, Smem& sm, unsigned char* r)
       : a(args), s(sm), ring(r), pol_stream(ptx::policy_evict_first()) {}
 
   __device__ bool confirm_oldest() {
     const int slot = rel % kSlots;
-    if (!wait_phase(&s.empty[slot], (rel / kSlots) & 1, &s.abort)) return false;
+    bool got = wait_phase(&s.empty[slot], (rel / kSlots) & 1, &s.abort);
+    if (kWarpCopy) got = __all_sync(kFull, got);   // the warp decides together
+    if (!got) return false;
     ++rel;
     head = rel < q ? static_cast<uint32_t>(s.info[rel % kSlots].off) : tail;
     return true;
@@ -213,20 +223,34 @@ struct Producer {
     }
   }
 
-  // Publishes item info and arms the slot's barrier for `bytes` of copies.
+  // Publishes item info and, for bulk copies, arms the slot's barrier for `bytes`.
   __device__ uint64_t* open(const Item& it, uint32_t bytes) {
     const int slot = q % kSlots;
     // The consumers' reads of this ring space are ordered before these copies by the
     // slot's empty barrier, which the producer has waited on.
-    s.info[slot] = it;
+    if (!kWarpCopy || lane == 0) s.info[slot] = it;
     tail = static_cast<uint32_t>(it.off) + bytes;
-    ptx::mbar_arrive_expect_tx(&s.full[slot], bytes);
+    if (!kWarpCopy) ptx::mbar_arrive_expect_tx(&s.full[slot], bytes);
     ++q;
     return &s.full[slot];
   }
 
   __device__ void copy(int dst_off, const void* src, uint32_t bytes, uint64_t* bar) {
-    ptx::bulk_g2s(ring + dst_off, src, bytes, bar, pol_stream);
+    if constexpr (kWarpCopy) {
+      const char* g = static_cast<const char*>(src);
+      for (uint32_t o = lane * 16u; o < bytes; o += 512u) ptx::cp_async16(ring + dst_off + o, g + o, pol_stream);
+    } else {
+      ptx::bulk_g2s(ring + dst_off, src, bytes, bar, pol_stream);
+    }
+  }
+
+  // Ends an item: with warp copies, each lane's arrival waits for its own copies, and
+  // lane 0 arrives once more to publish the item info.
+  __device__ void close(uint64_t* bar) {
+    if constexpr (kWarpCopy) {
+      ptx::cp_async_arrive_noinc(bar);
+      if (lane == 0) ptx::mbar_arrive(bar);
+    }
   }
 
   // One (chunk, column tile) item: the chunk's grad row segments, plus the main_grad
@@ -260,6 +284,7 @@ struct Producer {
       copy(off + len * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
            mg_bytes, bar);
     }
+    close(bar);
     return true;
   }
 
@@ -289,6 +314,7 @@ struct Producer {
         copy(off + nb * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
              mg_bytes, bar);
       }
+      close(bar);
     }
     return true;
   }
@@ -303,8 +329,10 @@ struct Producer {
     }
     if (ok) {
       const int slot = q % kSlots;
-      s.info[slot].kind = kEnd;
-      ptx::mbar_arrive(&s.full[slot]);
+      if (!kWarpCopy || lane == 0) s.info[slot].kind = kEnd;
+      if (kWarpCopy) __syncwarp();
+      ptx::mbar_arrive(&s.full[slot]);   // every producer lane (plus lane 0 below)
+      if (kWarpCopy && lane == 0) ptx::mbar_arrive(&s.full[slot]);
       ++q;
       return;
     }
@@ -369,7 +397,12 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   // claims increase).  Step k processes the item claimed at step k-3, whose entry was
   // fetched at step k-2, fetches the entry of the item claimed at step k-1 and claims
   // a new one.  The three slots are unrolled so each keeps its own registers.
-  auto claim = [&]() { return G + atomicAdd(work, 1); };
+  auto claim = [&]() {
+    int v = 0;
+    if (!kWarpCopy || (threadIdx.x & 31) == 0) v = G + atomicAdd(work, 1);
+    if (kWarpCopy) v = __shfl_sync(kFull, v, 0);
+    return v;
+  };
 
   int it[3];
   Desc d[3];
@@ -461,7 +494,7 @@ __global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
   const int t = threadIdx.x;
   if (t == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      ptx::mbar_init(&s.full[i], 1);
+      ptx::mbar_init(&s.full[i], kFullArrivals);
       ptx::mbar_init(&s.empty[i], kConsumerWarps);
     }
     ptx::fence_mbar_init();
@@ -515,7 +548,7 @@ __global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
   __syncthreads();
 
   if (t >= kConsumers) {
-    if (t == kConsumers) produce<GBF16, MBF16, LONG>(a, s, ring);
+    if (kWarpCopy || t == kConsumers) produce<GBF16, MBF16, LONG>(a, s, ring);
     return;
   }
   consume<GBF16, MBF16>(a, s, ring);

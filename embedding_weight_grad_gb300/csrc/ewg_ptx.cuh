@@ -62,6 +62,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through L2 (bypassing L1).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+               "l"(src), "l"(policy)
+               : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread has issued so far has landed; the
+// arrival is already counted in the barrier's expected count (.noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 // Bulk prefetch of global memory into L2 (normal eviction priority).  Address
 // 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
