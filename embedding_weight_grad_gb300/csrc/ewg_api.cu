@@ -198,6 +198,8 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
 
 }  // namespace
 
+void ewg::set_last_error(const char* msg) { g_last_error = msg; }
+
 extern "C" {
 
 int ewg_can_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const void* grad,

@@ -200,6 +200,9 @@ struct ApplyArgs {
   float* partial;
 };
 
+// Detail of the last error on the calling thread (read back by ewg_last_error).
+void set_last_error(const char* msg);
+
 // Host-side launchers.
 cudaError_t prepare_kernels();   // once per device, before the first launch
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);

@@ -145,6 +145,40 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride,
               int64_t num_embeddings, int64_t hidden, int64_t main_grad_row_stride,
               void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the library-owned scratch used by ewg_accumulate_static (64 MiB). */
+#define EWG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * ewg_accumulate without a caller workspace and without any allocation.  (The paper
+ * has no counterpart; this is an addition for callers that cannot allocate.)
+ *
+ * For callers that cannot allocate device memory when the gradient is accumulated:
+ * code running under a fixed-pool or custom allocator that must not grow, runtimes
+ * that forbid cudaMalloc after start-up, hooks called while a CUDA graph is being
+ * recorded.  The library keeps a file-scope __device__ array of
+ * EWG_STATIC_SCRATCH_BYTES as the workspace; every device that loads the library
+ * holds it until the process exits.  Arguments and results are those of
+ * ewg_accumulate, without the workspace.
+ *
+ * - Sizes whose ewg_workspace_bytes(num_tokens, hidden) exceeds
+ *   EWG_STATIC_SCRATCH_BYTES are rejected with EWG_ERR_UNSUPPORTED (and
+ *   ewg_last_error says so) before anything is enqueued.  64 MiB covers up to 8192
+ *   tokens for hidden sizes up to about 10000.
+ * - The call makes no cudaMalloc, cudaFree or other allocating call.  The first call on
+ *   a device looks up the array's device address with cudaGetSymbolAddress; make that
+ *   first call outside any stream capture.
+ * - Every call on a device uses the same array, which keeps the last call's contents
+ *   (nothing in it needs clearing between calls).  Calls that may overlap on the GPU
+ *   (different streams without ordering) race on it and must not be made.
+ * - If scratch_out is not NULL it receives the array's device address, which can be
+ *   passed to ewg_read_status to read the device status of the call.
+ */
+int ewg_accumulate_static(const void* ids, int ids_dtype, int64_t num_tokens,
+                          const void* grad, int grad_dtype, int64_t grad_row_stride,
+                          void* main_grad, int main_grad_dtype,
+                          int64_t num_embeddings, int64_t hidden,
+                          int64_t main_grad_row_stride, void* stream, void** scratch_out);
+
 /*
  * Waits for `stream`, then copies the device status of the last ewg_plan /
  * ewg_apply / ewg_accumulate that used this workspace into *status (EWG_OK,
