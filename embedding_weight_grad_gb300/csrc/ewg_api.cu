@@ -167,6 +167,7 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t H, voi
   a.hist = at<uint32_t>(ws, L.hist);
   a.tile_bad = at<int>(ws, L.tile_bad);
   a.tile_cnt = at<int4>(ws, L.tile_cnt);
+  a.arrivals = at<int>(ws, L.arrivals);
   cudaError_t e = ewg::launch_plan(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
   return EWG_OK;
@@ -191,6 +192,7 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.chunks = at<int>(ws, L.chunks);
   a.runs = at<int>(ws, L.runs);
   a.partial = at<float>(ws, L.partial);
+  a.arrivals = at<int>(ws, L.arrivals);
   cudaError_t e = ewg::launch_apply(a, grad_dtype == EWG_BF16, mg_dtype == EWG_BF16, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "apply launch");
   return EWG_OK;

@@ -1,4 +1,4 @@
-// Apply kernels: chunk partial sums, ordered long-run combine, add into main_grad.
+// Apply kernel: chunk partial sums, ordered long-run folds, add into main_grad.
 //
 // Counterpart of _partial_sums_kernel and _long_run_sums_kernel (Megatron Core API
 // docs, core.fusions.fused_embedding_wgrad, "Functions").  The arithmetic is the
@@ -7,18 +7,20 @@
 // order; w = round_to_grad_dtype(t); main_grad[id] = round_to_main_grad_dtype(
 // main_grad[id] + w) computed in fp32.
 //
-// Two persistent kernels, each a bulk-copy pipeline:
-//   apply_long   every (chunk of a long run, 1024-column tile): part -> fp32 partial row
-//   apply_rest   every (long run, 512-column group): fold the run's partial rows in
-//                chunk order, round, add into main_grad; then every (short run's
-//                chunk, 1024-column tile): part, round, add into main_grad
-// The kernel boundary orders every partial row before its fold, so no CTA waits for
-// another.  Within a CTA one producer thread issues cp.async.bulk copies of the
+// One persistent kernel, a bulk-copy pipeline per CTA, over three kinds of work item:
+//   long chunk   (chunk of a long run, column tile): part -> fp32 partial row
+//   fold         (long run, 512-column group): the run's partial rows in chunk order,
+//                round, add into main_grad
+//   short chunk  (chunk of a one-chunk run, column tile): part, round, add into main_grad
+// Items are handed out long chunks first and folds in the middle, so a fold's partial
+// rows are normally complete when it is claimed; a fold still waits (bounded) on its
+// run's arrival counter, which each consumer warp bumps after storing its partial
+// columns.  Within a CTA one producer thread issues cp.async.bulk copies of the
 // gathered grad row segments (or partial rows) and of the main_grad segment into a
-// 96 KB shared-memory ring, completing on a per-slot mbarrier; four consumer warps
-// (8 columns per thread) take the slots in order, add the rows in order from shared
-// memory and release the slot.  The depth of the ring, not the register file, sets
-// how many bytes each SM keeps in flight.
+// shared-memory ring, completing on a per-slot mbarrier; four consumer warps (8 columns
+// per thread) take the slots in order, add the rows in order from shared memory and
+// release the slot.  The depth of the ring, not the register file, sets how many bytes
+// each SM keeps in flight.
 #include <cuda_bf16.h>
 
 #include "ewg.h"
@@ -48,7 +50,7 @@ struct Item {
   int col0;       // first column
   int cols;       // columns
   int kind;
-  int flags;      // combine: bit 0 first batch, bit 1 last batch
+  int flags;      // fold: bit 0 first batch, bit 1 last batch; long chunk: its index c
 };
 
 struct Smem {
@@ -59,6 +61,7 @@ struct Smem {
   int offset[3][kMaxParts];
   int num_parts;
   int abort;
+  int epoch;      // apply calls already made on this plan
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -179,7 +182,7 @@ __device__ __forceinline__ int desc_pos(const Desc& d, int k) {
 }
 
 // The single producer thread of a CTA.
-template <bool GBF16, bool MBF16, bool LONG>
+template <bool GBF16, bool MBF16>
 struct Producer {
   const ApplyArgs& a;
   Smem& s;
@@ -255,19 +258,21 @@ struct Producer {
 
   // One (chunk, column tile) item: the chunk's grad row segments, plus the main_grad
   // segment when the run has no other chunk.
-  __device__ bool chunk_item(const Desc& d, int tile) {
-    const int tc = LONG ? a.tile_cols_long : a.tile_cols_rest;
+  __device__ bool chunk_item(const Desc& d, int tile, bool is_long) {
+    const int tc = is_long ? a.tile_cols_long : a.tile_cols_rest;
     const int col0 = tile * tc;
     const int cols = min(tc, a.hidden - col0);
     const int meta = d.w[2].w;
     const int len = meta & 15;
     const int id = d.w[2].z;
     const uint32_t row_bytes = cols * (GBF16 ? 2 : 4);
-    const uint32_t mg_bytes = LONG ? 0u : cols * (MBF16 ? 2 : 4);
+    const uint32_t mg_bytes = is_long ? 0u : cols * (MBF16 ? 2 : 4);
     const uint32_t bytes = len * row_bytes + mg_bytes;
     const int off = reserve(bytes);
     if (off < 0) return false;
-    Item it{off, len, id, d.w[3].x, col0, cols, LONG ? kLongChunk : kShortChunk, 0};
+    // for a long chunk, flags holds its index c in the run (prow - c: the run's counter)
+    Item it{off, len, id, d.w[3].x, col0, cols, is_long ? kLongChunk : kShortChunk,
+            is_long ? (meta >> 4) : 0};
     uint64_t* bar = open(it, bytes);
     const char* g = static_cast<const char*>(a.grad);
     const long long gsz = GBF16 ? 2 : 4;
@@ -278,7 +283,7 @@ struct Producer {
         copy(off + k * row_bytes, g + (p * a.grad_stride + col0) * gsz, row_bytes, bar);
       }
     }
-    if (!LONG) {
+    if (!is_long) {
       const char* m = static_cast<const char*>(a.main_grad);
       const long long msz = MBF16 ? 2 : 4;
       copy(off + len * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
@@ -288,10 +293,33 @@ struct Producer {
     return true;
   }
 
+  // Waits until every consumer warp that handled a chunk item of the run has stored its
+  // partial columns: C chunks x Tl column tiles x kConsumerWarps arrivals.  Bounded.
+  __device__ bool wait_run(int prow0, int target) {
+    const int* cnt = a.arrivals + prow0;
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+      int v;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+      if (v >= target) {
+        // the partial rows were written through the generic proxy; the bulk copies that
+        // read them run in the async proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        return true;
+      }
+      if ((i & 255u) == 255u && s.abort) return false;
+      __nanosleep(64);
+    }
+    return false;
+  }
+
   // One (long run, 512-column group) fold, as batches of partial rows; the last batch
   // also brings the main_grad segment.
-  __device__ bool combine_task(int4 run, int group) {
+  __device__ bool combine_task(int4 run, int group, int Tl) {
     const int prow0 = run.x, C = run.y, id = run.z;
+    if (!wait_run(prow0, (s.epoch + 1) * C * Tl * kConsumerWarps)) {
+      give_up(a, &s.abort);
+      return false;
+    }
     const int col0 = group * kCombineCols;
     const int cols = min(kCombineCols, a.hidden - col0);
     const uint32_t row_bytes = cols * 4;
@@ -345,68 +373,80 @@ struct Producer {
   }
 };
 
-template <bool GBF16, bool MBF16, bool LONG>
+template <bool GBF16, bool MBF16>
 __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
-  Producer<GBF16, MBF16, LONG> P(a, s, ring);
+  Producer<GBF16, MBF16> P(a, s, ring);
   const int parts = s.num_parts;
-  const int tc = LONG ? a.tile_cols_long : a.tile_cols_rest;
-  const int T = (a.hidden + tc - 1) / tc;
+  const int Tl = (a.hidden + a.tile_cols_long - 1) / a.tile_cols_long;
+  const int Ts = (a.hidden + a.tile_cols_rest - 1) / a.tile_cols_rest;
   const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
-  // Work items, in the order they are handed out: the chunk items, then (apply_rest
-  // only) the combine tasks, which wait for apply_long.  Counts fit in 32 bits
-  // (checked on the host).
-  const int list = LONG ? 0 : 1;
-  const int n_chunk_items = s.prefix[list][parts] * T;
-  const int n_tasks = LONG ? 0 : s.prefix[2][parts] * Tc;
-  const int first = n_chunk_items;
-  const int total = n_chunk_items + n_tasks;
-  int* work = const_cast<int*>(&a.header->work[LONG ? 0 : 1]);
+  // Work items, in the order they are handed out (counts fit in 32 bits, checked on the
+  // host).  The first G0 = min(G, short items) are the static first items of CTAs
+  // 0..G0-1; every other item is claimed from the kernel's counter, so a CTA owns a
+  // long-run chunk only once it is running.  A fold waits only for chunks handed out
+  // before it, each owned by a running CTA that processes its items in claim order and
+  // never waits on a chunk item: the waits end whether or not all CTAs are resident.
+  //   [0, G0)                short-run chunk items (static)
+  //   [G0, G0+L)             chunks of long runs, each over a column tile -> partial rows
+  //   [G0+L, G0+L+S1)        half of the other short-run chunk items
+  //   [G0+L+S1, G0+L+S1+F)   folds of the long runs (their partial rows are mostly done
+  //                          by then; a fold waits for the rest on the run's counter)
+  //   [G0+L+S1+F, L+S+F)     the remaining short-run chunk items
+  const int L = s.prefix[0][parts] * Tl;
+  const int S = s.prefix[1][parts] * Ts;
+  const int F = s.prefix[2][parts] * Tc;
   const int G = static_cast<int>(gridDim.x);
-  int cur_run = 0, cur_chunk = 0;
-  bool waited = LONG;   // apply_rest waits for apply_long before its first combine task
+  const int G0 = min(G, S);
+  const int S1 = (S - G0) / 2;
+  const int total = L + S + F;
+  int* work = const_cast<int*>(&a.header->work[0]);
+  int cur_long = 0, cur_short = 0, cur_run = 0;
 
-  // The entry an item needs: its chunk descriptor or its long-run table row.
-  // chunk-item ordinal of an item, or -1 for a combine task
-  auto chunk_ord = [&](int item) {
-    if (item < first) return item;
-    if (item < first + n_tasks) return -1;
-    return item - n_tasks;
+  // kind of an item and its ordinal within its list
+  auto classify = [&](int item, int& ord) {
+    if (item < G0) { ord = item; return kShortChunk; }
+    if (item < G0 + L) { ord = item - G0; return kLongChunk; }
+    if (item < G0 + L + S1) { ord = item - L; return kShortChunk; }
+    if (item < G0 + L + S1 + F) { ord = item - G0 - L - S1; return kCombine; }
+    ord = item - L - F;
+    return kShortChunk;
   };
+  // The entry an item needs: its chunk descriptor or its long-run table row.
   auto fetch = [&](int item) {
     Desc d{};
     if (item >= total) return d;
-    const int o = chunk_ord(item);
-    if (o >= 0) {
-      d = load_desc(a.chunks, list_index(s.prefix[list], s.offset[list], parts, o / T, cur_chunk));
+    int o = 0;
+    const int kind = classify(item, o);
+    if (kind == kLongChunk) {
+      d = load_desc(a.chunks, list_index(s.prefix[0], s.offset[0], parts, o / Tl, cur_long));
+    } else if (kind == kShortChunk) {
+      d = load_desc(a.chunks, list_index(s.prefix[1], s.offset[1], parts, o / Ts, cur_short));
     } else {
-      const int ri = list_index(s.prefix[2], s.offset[2], parts, (item - first) / Tc, cur_run);
+      const int ri = list_index(s.prefix[2], s.offset[2], parts, o / Tc, cur_run);
       d.w[0] = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
     }
     return d;
   };
   auto run_item = [&](int item, const Desc& d) {
-    const int o = chunk_ord(item);
-    if (o >= 0) return P.chunk_item(d, o % T);
-    if (!waited) {   // the partial rows are apply_long's output
-      ptx::pdl_wait_prior_grid();
-      waited = true;
-    }
-    return P.combine_task(d.w[0], (item - first) % Tc);
+    int o = 0;
+    const int kind = classify(item, o);
+    if (kind == kLongChunk) return P.chunk_item(d, o % Tl, true);
+    if (kind == kShortChunk) return P.chunk_item(d, o % Ts, false);
+    return P.combine_task(d.w[0], o % Tc, Tl);
   };
-  // Claims: item blockIdx.x first, then G + the kernel's counter, one at a time (a CTA's
-  // claims increase).  Step k processes the item claimed at step k-3, whose entry was
-  // fetched at step k-2, fetches the entry of the item claimed at step k-1 and claims
-  // a new one.  The three slots are unrolled so each keeps its own registers.
+  // Claims increase within a CTA.  Step k processes the item claimed at step k-3, whose
+  // entry was fetched at step k-2, fetches the entry of the item claimed at step k-1
+  // and claims a new one.  The three slots are unrolled so each keeps its own registers.
   auto claim = [&]() {
     int v = 0;
-    if (!kWarpCopy || (threadIdx.x & 31) == 0) v = G + atomicAdd(work, 1);
+    if (!kWarpCopy || (threadIdx.x & 31) == 0) v = G0 + atomicAdd(work, 1);
     if (kWarpCopy) v = __shfl_sync(kFull, v, 0);
     return v;
   };
 
   int it[3];
   Desc d[3];
-  it[0] = blockIdx.x;
+  it[0] = static_cast<int>(blockIdx.x) < G0 ? static_cast<int>(blockIdx.x) : claim();
   it[1] = claim();
   it[2] = claim();
   d[0] = fetch(it[0]);
@@ -427,8 +467,6 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
     }
   }
   P.finish_stream();
-  // every CTA waits, so this grid never completes before the previous one
-  if (!waited) ptx::pdl_wait_prior_grid();
 }
 
 template <bool GBF16, bool MBF16>
@@ -480,14 +518,19 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
                                it.col0 + c);
         }
       }
+      if (it.kind == kLongChunk) {   // publish this warp's partial columns to the fold
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(a.arrivals + (it.prow - it.flags), 1);
+      }
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&s.empty[slot]);
   }
 }
 
-template <bool GBF16, bool MBF16, bool LONG>
-__global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
+template <bool GBF16, bool MBF16>
+__global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(ApplyArgs a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
   Smem& s = *reinterpret_cast<Smem*>(smem_raw + kRingBytes);
@@ -500,14 +543,9 @@ __global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
     ptx::fence_mbar_init();
     s.abort = 0;
   }
-  // apply_long waits for the plan.  apply_rest is launched only once every apply_long
-  // CTA has passed that wait, so the plan is complete and visible to it; it waits for
-  // apply_long itself only before reading partial rows (and, like every CTA of both
-  // kernels, before it exits, so neither grid completes before its predecessor).
-  if (LONG) {
-    ptx::pdl_wait_prior_grid();
-    ptx::pdl_launch_dependents();
-  }
+  // Launched early on the SMs the plan leaves free; the plan's lists are read only
+  // after it has completed.
+  ptx::pdl_wait_prior_grid();
 
   const Header* h = a.header;
   if (t == 0) {   // one reader decides for the whole CTA
@@ -517,12 +555,10 @@ __global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
       go = 0;
     }
     s.num_parts = go ? h->num_parts : -1;
+    s.epoch = h->epoch;
   }
   __syncthreads();
-  if (s.num_parts < 0) {
-    if (!LONG) ptx::pdl_wait_prior_grid();
-    return;
-  }
+  if (s.num_parts < 0) return;
   if (t < 32) {   // partition tables -> per-list prefix counts
     const int parts = s.num_parts;
     for (int list = 0; list < 3; ++list) {
@@ -548,35 +584,35 @@ __global__ void __launch_bounds__(kApplyThreads, 2) apply_kernel(ApplyArgs a) {
   __syncthreads();
 
   if (t >= kConsumers) {
-    if (kWarpCopy || t == kConsumers) produce<GBF16, MBF16, LONG>(a, s, ring);
+    if (kWarpCopy || t == kConsumers) produce<GBF16, MBF16>(a, s, ring);
     return;
   }
   consume<GBF16, MBF16>(a, s, ring);
-  // The last CTA to finish re-arms the kernel's work counter, so that one plan can
-  // serve further ewg_apply calls.  Every CTA claims its last item before its
-  // consumers see the end of its stream, so no claim can follow this reset.
+  // The last CTA to finish re-arms the work counter and the long runs' arrival counters,
+  // so that one plan can serve further ewg_apply calls.  Every CTA claims its last item
+  // before its consumers see the end of its stream, so no claim can follow this reset.
   if (t == 0) {
     Header* hw = const_cast<Header*>(h);
-    const int k = LONG ? 0 : 1;
-    if (atomicAdd(&hw->done[k], 1) == static_cast<int>(gridDim.x) - 1) {
-      hw->work[k] = 0;
-      hw->done[k] = 0;
+    if (atomicAdd(&hw->done, 1) == static_cast<int>(gridDim.x) - 1) {
+      hw->work[0] = 0;
+      hw->done = 0;
+      hw->epoch = s.epoch + 1;   // the arrival counters of the next call start here
     }
   }
 }
 
 constexpr size_t kApplySmem = kRingBytes + sizeof(Smem);
 
-template <bool G, bool M, bool LONG>
+template <bool G, bool M>
 cudaError_t launch_one(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
   static int blocks_per_sm = 0;
   if (blocks_per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(apply_kernel<G, M, LONG>,
+    cudaError_t e = cudaFuncSetAttribute(apply_kernel<G, M>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kApplySmem));
     if (e != cudaSuccess) return e;
     int b = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, apply_kernel<G, M, LONG>, kApplyThreads,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, apply_kernel<G, M>, kApplyThreads,
                                                       kApplySmem);
     if (e != cudaSuccess) return e;
     blocks_per_sm = b > 0 ? b : 1;
@@ -591,14 +627,7 @@ cudaError_t launch_one(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, apply_kernel<G, M, LONG>, a);
-}
-
-template <bool G, bool M>
-cudaError_t launch_pair(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
-  cudaError_t e = launch_one<G, M, true>(a, num_sms, stream);
-  if (e != cudaSuccess) return e;
-  return launch_one<G, M, false>(a, num_sms, stream);
+  return cudaLaunchKernelEx(&cfg, apply_kernel<G, M>, a);
 }
 
 }  // namespace
@@ -606,11 +635,11 @@ cudaError_t launch_pair(const ApplyArgs& a, int num_sms, cudaStream_t stream) {
 cudaError_t launch_apply(const ApplyArgs& a, int grad_bf16, int mg_bf16, int num_sms,
                          cudaStream_t stream) {
   if (grad_bf16) {
-    return mg_bf16 ? launch_pair<true, true>(a, num_sms, stream)
-                   : launch_pair<true, false>(a, num_sms, stream);
+    return mg_bf16 ? launch_one<true, true>(a, num_sms, stream)
+                   : launch_one<true, false>(a, num_sms, stream);
   }
-  return mg_bf16 ? launch_pair<false, true>(a, num_sms, stream)
-                 : launch_pair<false, false>(a, num_sms, stream);
+  return mg_bf16 ? launch_one<false, true>(a, num_sms, stream)
+                 : launch_one<false, false>(a, num_sms, stream);
 }
 
 }  // namespace ewg

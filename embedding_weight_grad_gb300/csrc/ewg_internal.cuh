@@ -54,22 +54,22 @@ constexpr int kTileThreads = 256;
 constexpr int kTileItems = 8;
 constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
 
-// Apply kernels.  Bulk copies reach full HBM bandwidth only from about 4 KB up, so an
-// item covers whole rows: a chunk over a column tile of up to 8192 columns (4096 for
-// an fp32 gradient), each grad row and the main_grad row one copy.
-constexpr int kMaxTileColsBf16 = 4096;
-constexpr int kMaxTileColsFp32 = 2048;
+// Apply kernel.  Bulk copies reach full HBM bandwidth only from about 4 KB up, so an
+// item covers a chunk over a column tile of up to 2048 columns (1024 for an fp32
+// gradient), each grad row segment and the main_grad segment one copy.
+constexpr int kMaxTileColsBf16 = 2048;
+constexpr int kMaxTileColsFp32 = 1024;
 constexpr int kCombineCols = 512;     // columns of one combine task (2 KB partial rows)
 constexpr int kCombineBatch = 8;      // partial rows per combine ring item
-constexpr int kConsumerWarps = 8;
+constexpr int kApplyCtasPerSm = 4;    // independent copy-issuing streams per SM
+constexpr int kConsumerWarps = 4;
 constexpr int kConsumers = kConsumerWarps * 32;           // 8 columns each per pass
 constexpr int kApplyThreads = kConsumers + 32;            // + one producer warp
-constexpr int kRingBytes = 100 * 1024;
+constexpr int kRingBytes = 50 * 1024;
 constexpr int kSlots = 16;
 
-// Long-run chunks carry 10 rows, so their items use tiles of at most 4096 columns:
-// twice as many, half-size items keep the end of apply_long short.
-constexpr int kMaxLongTileCols = 4096;
+// Column limit of a long-run chunk item (it carries 10 rows).
+constexpr int kMaxLongTileCols = 2048;
 
 // Column tile of the chunk items: the widest tile within the limit, split evenly.
 inline int tile_cols(int64_t hidden, bool grad_bf16, bool long_chunks) {
@@ -89,8 +89,9 @@ struct Header {
   int num_parts;
   long long num_embeddings;
   int bad_ids;
-  int work[2];           // next item of apply_long / apply_rest (zeroed by the plan)
-  int done[2];           // CTAs of apply_long / apply_rest that have finished
+  int work[2];           // next work item of the apply kernel (zeroed by the plan)
+  int done;              // apply CTAs that have finished (zeroed by the plan)
+  int epoch;             // apply calls completed on this plan (zeroed by the plan)
   int pad[53];
 };
 static_assert(sizeof(Header) == 256, "header is one 256-byte region");
@@ -104,7 +105,7 @@ inline int64_t max_partial_rows(int64_t n) { return 2 * n / 11 + kMaxParts + 1; 
 inline int64_t max_long_runs(int64_t n) { return n / 11 + kMaxParts + 1; }
 
 struct Layout {
-  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, hist, tile_bad, tile_cnt,
+  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, hist, tile_bad, tile_cnt, arrivals,
       partial, total;
   int64_t n, hidden, tiles;
 };
@@ -132,6 +133,7 @@ inline Layout make_layout(int64_t n, int64_t hidden) {
   L.hist = take(static_cast<size_t>(L.tiles) * (1 << kMaxDigitBits) * 4);
   L.tile_bad = take(static_cast<size_t>(L.tiles) * 4);
   L.tile_cnt = take(static_cast<size_t>(L.tiles) * 16);
+  L.arrivals = take(static_cast<size_t>(max_partial_rows(n)) * 4);
   L.partial = take(static_cast<size_t>(max_partial_rows(n)) * hidden * 4);
   L.total = off;
   return L;
@@ -181,6 +183,7 @@ struct PlanArgs {
   uint32_t* hist;
   int* tile_bad;
   int4* tile_cnt;        // per tile: long chunks, short chunks, long runs
+  int* arrivals;         // per long run, at its first partial row: zeroed here
 };
 
 struct ApplyArgs {
@@ -198,6 +201,7 @@ struct ApplyArgs {
   const int* chunks;
   const int* runs;
   float* partial;
+  int* arrivals;           // per long run (at its first partial row): finished chunk parts
 };
 
 // Detail of the last error on the calling thread (read back by ewg_last_error).
@@ -206,8 +210,7 @@ void set_last_error(const char* msg);
 // Host-side launchers.
 cudaError_t prepare_kernels();   // once per device, before the first launch
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
-// apply_long then apply_rest, each chained to its predecessor by programmatic
-// dependent launch.
+// The apply kernel, chained to its predecessor by programmatic dependent launch.
 cudaError_t launch_apply(const ApplyArgs& a, int grad_bf16, int mg_bf16, int num_sms,
                          cudaStream_t stream);
 

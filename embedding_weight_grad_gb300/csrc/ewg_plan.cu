@@ -251,6 +251,7 @@ struct Listing {
       if (is_long) {
         if (c == 0) {
           reinterpret_cast<int4*>(a.runs)[b.run + ri] = make_int4(prow, C, static_cast<int>(key[i]), 0);
+          a.arrivals[prow] = 0;
           ++ri;
         }
         ++li;
@@ -269,7 +270,8 @@ __device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
   h->num_parts = num_parts;
   h->bad_ids = bad;
   h->work[0] = h->work[1] = 0;
-  h->done[0] = h->done[1] = 0;
+  h->done = 0;
+  h->epoch = 0;
   h->status = bad ? EWG_ERR_ID_OUT_OF_RANGE : EWG_OK;
 }
 
@@ -458,6 +460,7 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
         tbase[s] = static_cast<uint32_t>(long_desc + li);
         reinterpret_cast<int4*>(a.runs)[run_base + ri] =
             make_int4(partial_base + li, C, static_cast<int>(tkey[s]), 0);
+        a.arrivals[partial_base + li] = 0;
         li += C;
         ++ri;
       } else if (L > 0) {
