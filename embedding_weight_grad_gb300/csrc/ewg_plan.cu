@@ -299,6 +299,10 @@ constexpr int kHashWarps = kHashThreads / 32;
 constexpr int kTableMax = kHashMaxN;           // table slots at most (a power of two)
 constexpr uint32_t kEmptySlot = 0xffffffffu;
 constexpr int kRankShift = 13;                 // key info word: slot | rank << 13
+constexpr uint32_t kSlotMask = (1u << kRankShift) - 1u;
+// key info word between the probe and the ranks: slot | rank in the 32-key group |
+// lane of the group's last key of the id | that id's keys in the group - 1
+constexpr int kInRankShift = 13, kLastShift = 18, kGroupCntShift = 23;
 static_assert(kTableMax <= (1 << kRankShift) && kHashMaxN <= (1 << (32 - kRankShift)),
               "slot and rank must pack into one word");
 constexpr size_t kHashSmem =
@@ -414,23 +418,34 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
       }
     }
     h = __shfl_sync(kFull, h, leader);
-    if (valid) kinfo[i] = h;
+    // the key's rank among its group's keys of the same id, the group's last such key
+    // and their number
+    if (valid)
+      kinfo[i] = h | (static_cast<uint32_t>(__popc(peers & lt)) << kInRankShift) |
+                 (static_cast<uint32_t>(31 - __clz(peers)) << kLastShift) |
+                 (static_cast<uint32_t>(__popc(peers) - 1) << kGroupCntShift);
   }
   __syncthreads();
 
-  // 4. ranks in position order, one warp, 32 keys per step
+  // 4. ranks in position order: one warp carries the per-slot counts across the 32-key
+  // groups in order; each group's last key of an id adds the group's count
   if (warp == 0) {
+    uint32_t next = lane < m ? kinfo[lane] : 0u;
     for (int i0 = 0; i0 < m; i0 += 32) {
       const int i = i0 + lane;
       const bool valid = i < m;
-      const uint32_t s = valid ? kinfo[i] : kEmptySlot;
-      const unsigned peers = __match_any_sync(kFull, s);
+      const uint32_t info = next;
+      next = i + 32 < m ? kinfo[i + 32] : 0u;
+      const uint32_t s = info & kSlotMask;
+      const int last = static_cast<int>((info >> kLastShift) & 31u);
       uint32_t prior = 0;
-      if (valid) prior = tcnt[s];
+      if (valid && lane == last) {
+        prior = tcnt[s];
+        tcnt[s] = prior + ((info >> kGroupCntShift) & 31u) + 1u;
+      }
       __syncwarp();
-      if (valid && lane == 31 - __clz(peers)) tcnt[s] = prior + __popc(peers);
-      __syncwarp();
-      if (valid) kinfo[i] = s | ((prior + __popc(peers & lt)) << kRankShift);
+      const uint32_t base = __shfl_sync(kFull, prior, last);
+      if (valid) kinfo[i] = s | ((base + ((info >> kInRankShift) & 31u)) << kRankShift);
     }
   }
   __syncthreads();
