@@ -15,11 +15,11 @@
 // Items are handed out long chunks first and folds in the middle, so a fold's partial
 // rows are normally complete when it is claimed; a fold still waits (bounded) on its
 // run's arrival counter, which each consumer warp bumps after storing its partial
-// columns.  Within a CTA one producer thread issues cp.async.bulk copies of the
-// gathered grad row segments (or partial rows) and of the main_grad segment into a
-// shared-memory ring, completing on a per-slot mbarrier; four consumer warps (8 columns
-// per thread) take the slots in order, add the rows in order from shared memory and
-// release the slot.  The depth of the ring, not the register file, sets how many bytes
+// columns.  Within a CTA a producer warp issues cp.async.bulk copies of the gathered
+// grad row segments (or partial rows) and of the main_grad segment into a shared-memory
+// ring, one lane per row, completing on a per-slot mbarrier; four consumer warps (8
+// columns per thread) take the slots in order, add the rows in order from shared memory
+// and release the slot.  The depth of the ring, not the register file, sets how many bytes
 // each SM keeps in flight.
 #include <cuda_bf16.h>
 
@@ -35,12 +35,13 @@ constexpr uint32_t kSpinLimit = 1u << 22;   // bounded mbarrier waits
 
 enum ItemKind { kEnd = -1, kShortChunk = 0, kLongChunk = 1, kCombine = 2 };
 
-// How the producer fills the ring: with one thread issuing cp.async.bulk (TMA) copies,
-// or with the whole producer warp issuing 16-byte cp.async copies (512 bytes per
-// instruction, completion tracked per lane on the slot's barrier).  Measured on the
-// large-vocabulary workload the bulk copies are faster, so they are the ones built.
-constexpr bool kWarpCopy = false;
-constexpr int kFullArrivals = kWarpCopy ? 33 : 1;   // 32 lanes + the info publisher
+// The producer's lookahead: an item is claimed kClaimAhead steps before its table entry
+// is staged in shared memory, and staged kStageAhead steps before it is issued, so
+// neither the claim (an atomic on a counter all CTAs share) nor the entry's load stalls
+// the issue.
+constexpr int kClaimAhead = 3;
+constexpr int kStageAhead = 2;
+constexpr int kStage = kStageAhead + 1;   // staged entries: in flight + the one issued
 
 struct Item {
   int off;        // byte offset of the item in the ring
@@ -54,6 +55,9 @@ struct Item {
 };
 
 struct Smem {
+  int4 desc[kStage][kChunkWords / 4];   // staged chunk descriptors / long-run rows
+  int kind[kStage];                     // the staged items' kinds ...
+  int tile[kStage];                     // ... and column tiles (fold: column group)
   uint64_t full[kSlots];
   uint64_t empty[kSlots];
   Item info[kSlots];
@@ -157,51 +161,32 @@ __device__ __forceinline__ int list_index(const int* prefix, const int* offset, 
   return offset[cur] + (ord - prefix[cur]);
 }
 
-struct Desc {
-  int4 w[4];
-};
-
-__device__ __forceinline__ Desc load_desc(const int* chunks, int di) {
-  const int4* p = reinterpret_cast<const int4*>(chunks + static_cast<long long>(di) * kChunkWords);
-  Desc d;
-  d.w[0] = __ldg(p);
-  d.w[1] = __ldg(p + 1);
-  d.w[2] = __ldg(p + 2);
-  d.w[3] = __ldg(p + 3);
-  return d;
-}
-
-__device__ __forceinline__ int desc_pos(const Desc& d, int k) {
-  const int4& v = d.w[k >> 2];
-  switch (k & 3) {
-    case 0: return v.x;
-    case 1: return v.y;
-    case 2: return v.z;
-    default: return v.w;
-  }
-}
-
-// The single producer thread of a CTA.
+// The producer warp of a CTA.  Its 32 lanes take the same steps in lockstep, so every
+// lane holds the same ring bookkeeping; lane 0 publishes item info and arms the slot
+// barriers, and the lanes issue the bulk copies of an item's rows side by side (lane k
+// copies row k), which keeps the serial instruction path per item short.
 template <bool GBF16, bool MBF16>
 struct Producer {
   const ApplyArgs& a;
   Smem& s;
   unsigned char* ring;
+  const int lane;
   int q = 0;            // items issued
   int rel = 0;          // items known to be consumed
   uint32_t head = 0, tail = 0;
-  uint64_t pol_stream;
+  uint64_t pol;
   bool ok = true;
-  const uint32_t lane = threadIdx.x & 31;
 
   __device__ Producer(const ApplyArgs& args, Smem& sm, unsigned char* r)
-      : a(args), s(sm), ring(r), pol_stream(ptx::policy_evict_first()) {}
+      : a(args), s(sm), ring(r), lane(static_cast<int>(threadIdx.x & 31)),
+        pol(ptx::policy_evict_first()) {}
 
+  // Lane 0 waits (bounded) for the oldest item in the ring to be consumed.
   __device__ bool confirm_oldest() {
     const int slot = rel % kSlots;
-    bool got = wait_phase(&s.empty[slot], (rel / kSlots) & 1, &s.abort);
-    if (kWarpCopy) got = __all_sync(kFull, got);   // the warp decides together
-    if (!got) return false;
+    int got = 0;
+    if (lane == 0) got = wait_phase(&s.empty[slot], (rel / kSlots) & 1, &s.abort);
+    if (!__shfl_sync(kFull, got, 0)) return false;
     ++rel;
     head = rel < q ? static_cast<uint32_t>(s.info[rel % kSlots].off) : tail;
     return true;
@@ -226,98 +211,86 @@ struct Producer {
     }
   }
 
-  // Publishes item info and, for bulk copies, arms the slot's barrier for `bytes`.
+  // Publishes the item and arms its slot's barrier for `bytes`; the copies follow.
   __device__ uint64_t* open(const Item& it, uint32_t bytes) {
     const int slot = q % kSlots;
-    // The consumers' reads of this ring space are ordered before these copies by the
-    // slot's empty barrier, which the producer has waited on.
-    if (!kWarpCopy || lane == 0) s.info[slot] = it;
+    // The consumers' reads of this ring space are ordered before the new copies by the
+    // slot's empty barrier, which lane 0 has waited on.
+    if (lane == 0) {
+      s.info[slot] = it;
+      ptx::mbar_arrive_expect_tx(&s.full[slot], bytes);
+    }
+    __syncwarp();
     tail = static_cast<uint32_t>(it.off) + bytes;
-    if (!kWarpCopy) ptx::mbar_arrive_expect_tx(&s.full[slot], bytes);
     ++q;
     return &s.full[slot];
   }
 
-  __device__ void copy(int dst_off, const void* src, uint32_t bytes, uint64_t* bar) {
-    if constexpr (kWarpCopy) {
-      const char* g = static_cast<const char*>(src);
-      for (uint32_t o = lane * 16u; o < bytes; o += 512u) ptx::cp_async16(ring + dst_off + o, g + o, pol_stream);
-    } else {
-      ptx::bulk_g2s(ring + dst_off, src, bytes, bar, pol_stream);
-    }
-  }
-
-  // Ends an item: with warp copies, each lane's arrival waits for its own copies, and
-  // lane 0 arrives once more to publish the item info.
-  __device__ void close(uint64_t* bar) {
-    if constexpr (kWarpCopy) {
-      ptx::cp_async_arrive_noinc(bar);
-      if (lane == 0) ptx::mbar_arrive(bar);
-    }
-  }
-
-  // One (chunk, column tile) item: the chunk's grad row segments, plus the main_grad
-  // segment when the run has no other chunk.
-  __device__ bool chunk_item(const Desc& d, int tile, bool is_long) {
+  // One (chunk, column tile) item: the chunk's grad row segments (lane k: row k), plus
+  // the main_grad segment (lane len) when the run has no other chunk.
+  __device__ bool chunk_item(const int* d, int tile, bool is_long) {
     const int tc = is_long ? a.tile_cols_long : a.tile_cols_rest;
     const int col0 = tile * tc;
     const int cols = min(tc, a.hidden - col0);
-    const int meta = d.w[2].w;
+    const int meta = d[kDescMeta];
     const int len = meta & 15;
-    const int id = d.w[2].z;
+    const int id = d[kDescId];
     const uint32_t row_bytes = cols * (GBF16 ? 2 : 4);
     const uint32_t mg_bytes = is_long ? 0u : cols * (MBF16 ? 2 : 4);
     const uint32_t bytes = len * row_bytes + mg_bytes;
     const int off = reserve(bytes);
     if (off < 0) return false;
     // for a long chunk, flags holds its index c in the run (prow - c: the run's counter)
-    Item it{off, len, id, d.w[3].x, col0, cols, is_long ? kLongChunk : kShortChunk,
+    Item it{off, len, id, d[kDescPartial], col0, cols, is_long ? kLongChunk : kShortChunk,
             is_long ? (meta >> 4) : 0};
     uint64_t* bar = open(it, bytes);
-    const char* g = static_cast<const char*>(a.grad);
-    const long long gsz = GBF16 ? 2 : 4;
-#pragma unroll
-    for (int k = 0; k < kNrows; ++k) {
-      if (k < len) {
-        const long long p = desc_pos(d, k);
-        copy(off + k * row_bytes, g + (p * a.grad_stride + col0) * gsz, row_bytes, bar);
-      }
-    }
-    if (!is_long) {
+    if (lane < len) {
+      const long long p = d[kDescPos + lane];
+      const char* g = static_cast<const char*>(a.grad);
+      ptx::bulk_g2s(ring + off + lane * row_bytes, g + (p * a.grad_stride + col0) * (GBF16 ? 2 : 4),
+                    row_bytes, bar, pol);
+    } else if (lane == len && !is_long) {
       const char* m = static_cast<const char*>(a.main_grad);
-      const long long msz = MBF16 ? 2 : 4;
-      copy(off + len * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
-           mg_bytes, bar);
+      ptx::bulk_g2s(ring + off + len * row_bytes,
+                    m + (static_cast<long long>(id) * a.mg_stride + col0) * (MBF16 ? 2 : 4), mg_bytes,
+                    bar, pol);
     }
-    close(bar);
     return true;
   }
 
   // Waits until every consumer warp that handled a chunk item of the run has stored its
-  // partial columns: C chunks x Tl column tiles x kConsumerWarps arrivals.  Bounded.
+  // partial columns: C chunks x Tl column tiles x kConsumerWarps arrivals.  Lane 0 spins
+  // (bounded); then every lane acquires the counter itself, so its later bulk copies of
+  // the partial rows (async proxy) come after the rows' generic-proxy stores.
   __device__ bool wait_run(int prow0, int target) {
     const int* cnt = a.arrivals + prow0;
-    for (uint32_t i = 0; i < kSpinLimit; ++i) {
-      int v;
-      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-      if (v >= target) {
-        // the partial rows were written through the generic proxy; the bulk copies that
-        // read them run in the async proxy
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        return true;
+    int got = 0;
+    if (lane == 0) {
+      for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+        if (v >= target) {
+          got = 1;
+          break;
+        }
+        if ((i & 255u) == 255u && s.abort) break;
+        __nanosleep(64);
       }
-      if ((i & 255u) == 255u && s.abort) return false;
-      __nanosleep(64);
     }
-    return false;
+    if (!__shfl_sync(kFull, got, 0)) return false;
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    (void)v;
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    return true;
   }
 
-  // One (long run, 512-column group) fold, as batches of partial rows; the last batch
-  // also brings the main_grad segment.
-  __device__ bool combine_task(int4 run, int group, int Tl) {
-    const int prow0 = run.x, C = run.y, id = run.z;
+  // One (long run, 512-column group) fold, as batches of partial rows (lane k: row k of
+  // the batch); the last batch also brings the main_grad segment.
+  __device__ bool combine_task(const int* run, int group, int Tl) {
+    const int prow0 = run[0], C = run[1], id = run[2];
     if (!wait_run(prow0, (s.epoch + 1) * C * Tl * kConsumerWarps)) {
-      give_up(a, &s.abort);
+      if (lane == 0) give_up(a, &s.abort);
       return false;
     }
     const int col0 = group * kCombineCols;
@@ -332,17 +305,15 @@ struct Producer {
       if (off < 0) return false;
       Item it{off, nb, id, -1, col0, cols, kCombine, (b0 == 0 ? 1 : 0) | (last ? 2 : 0)};
       uint64_t* bar = open(it, bytes);
-      for (int k = 0; k < nb; ++k) {
-        const float* src = a.partial + static_cast<long long>(prow0 + b0 + k) * a.hidden + col0;
-        copy(off + k * row_bytes, src, row_bytes, bar);
-      }
-      if (last) {
+      if (lane < nb) {
+        const float* src = a.partial + static_cast<long long>(prow0 + b0 + lane) * a.hidden + col0;
+        ptx::bulk_g2s(ring + off + lane * row_bytes, src, row_bytes, bar, pol);
+      } else if (lane == nb && last) {
         const char* m = static_cast<const char*>(a.main_grad);
-        const long long msz = MBF16 ? 2 : 4;
-        copy(off + nb * row_bytes, m + (static_cast<long long>(id) * a.mg_stride + col0) * msz,
-             mg_bytes, bar);
+        ptx::bulk_g2s(ring + off + nb * row_bytes,
+                      m + (static_cast<long long>(id) * a.mg_stride + col0) * (MBF16 ? 2 : 4),
+                      mg_bytes, bar, pol);
       }
-      close(bar);
     }
     return true;
   }
@@ -356,18 +327,20 @@ struct Producer {
         }
     }
     if (ok) {
-      const int slot = q % kSlots;
-      if (!kWarpCopy || lane == 0) s.info[slot].kind = kEnd;
-      if (kWarpCopy) __syncwarp();
-      ptx::mbar_arrive(&s.full[slot]);   // every producer lane (plus lane 0 below)
-      if (kWarpCopy && lane == 0) ptx::mbar_arrive(&s.full[slot]);
+      if (lane == 0) {
+        const int slot = q % kSlots;
+        s.info[slot].kind = kEnd;
+        ptx::mbar_arrive(&s.full[slot]);
+      }
       ++q;
       return;
     }
     // gave up: let the copies already in flight land before the CTA exits
-    for (int r = rel; r < q; ++r) {
-      uint64_t* bar = &s.full[r % kSlots];
-      for (uint32_t i = 0; i < kSpinLimit && !ptx::mbar_try_wait(bar, (r / kSlots) & 1); ++i) {
+    if (lane == 0) {
+      for (int r = rel; r < q; ++r) {
+        uint64_t* bar = &s.full[r % kSlots];
+        for (uint32_t i = 0; i < kSpinLimit && !ptx::mbar_try_wait(bar, (r / kSlots) & 1); ++i) {
+        }
       }
     }
   }
@@ -376,6 +349,7 @@ struct Producer {
 template <bool GBF16, bool MBF16>
 __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   Producer<GBF16, MBF16> P(a, s, ring);
+  const int lane = P.lane;
   const int parts = s.num_parts;
   const int Tl = (a.hidden + a.tile_cols_long - 1) / a.tile_cols_long;
   const int Ts = (a.hidden + a.tile_cols_rest - 1) / a.tile_cols_rest;
@@ -400,72 +374,88 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int S1 = (S - G0) / 2;
   const int total = L + S + F;
   int* work = const_cast<int*>(&a.header->work[0]);
-  int cur_long = 0, cur_short = 0, cur_run = 0;
+  int cur0 = 0, cur1 = 0, cur2 = 0;   // list cursors (ordinals increase along the claims)
 
-  // kind of an item and its ordinal within its list
-  auto classify = [&](int item, int& ord) {
-    if (item < G0) { ord = item; return kShortChunk; }
-    if (item < G0 + L) { ord = item - G0; return kLongChunk; }
-    if (item < G0 + L + S1) { ord = item - L; return kShortChunk; }
-    if (item < G0 + L + S1 + F) { ord = item - G0 - L - S1; return kCombine; }
-    ord = item - L - F;
-    return kShortChunk;
-  };
-  // The entry an item needs: its chunk descriptor or its long-run table row.
-  auto fetch = [&](int item) {
-    Desc d{};
-    if (item >= total) return d;
-    int o = 0;
-    const int kind = classify(item, o);
-    if (kind == kLongChunk) {
-      d = load_desc(a.chunks, list_index(s.prefix[0], s.offset[0], parts, o / Tl, cur_long));
-    } else if (kind == kShortChunk) {
-      d = load_desc(a.chunks, list_index(s.prefix[1], s.offset[1], parts, o / Ts, cur_short));
-    } else {
-      const int ri = list_index(s.prefix[2], s.offset[2], parts, o / Tc, cur_run);
-      d.w[0] = __ldg(reinterpret_cast<const int4*>(a.runs) + ri);
+  // Stages the table entry of `item` (its chunk descriptor, or its long-run row) in
+  // shared-memory stage `st` with asynchronous copies (one commit group per lane and
+  // call), and records the item's kind and column tile (or fold group).
+  auto stage = [&](int item, int st) {
+    __syncwarp();   // every lane's reads of this stage's previous entry are done
+    int kind = kEnd, tile = 0;
+    if (item < total) {
+      int o;
+      if (item < G0) { kind = kShortChunk; o = item; }
+      else if (item < G0 + L) { kind = kLongChunk; o = item - G0; }
+      else if (item < G0 + L + S1) { kind = kShortChunk; o = item - L; }
+      else if (item < G0 + L + S1 + F) { kind = kCombine; o = item - G0 - L - S1; }
+      else { kind = kShortChunk; o = item - L - F; }
+      const int list = kind == kLongChunk ? 0 : kind == kShortChunk ? 1 : 2;
+      const int T = list == 0 ? Tl : list == 1 ? Ts : Tc;
+      const int e = o / T;
+      tile = o - e * T;
+      const int idx = list == 0   ? list_index(s.prefix[0], s.offset[0], parts, e, cur0)
+                      : list == 1 ? list_index(s.prefix[1], s.offset[1], parts, e, cur1)
+                                  : list_index(s.prefix[2], s.offset[2], parts, e, cur2);
+      if (kind == kCombine) {
+        if (lane == 0) ptx::cp_async16(&s.desc[st][0], reinterpret_cast<const int4*>(a.runs) + idx, P.pol);
+      } else if (lane < kChunkWords / 4) {
+        const int4* src = reinterpret_cast<const int4*>(a.chunks + static_cast<long long>(idx) * kChunkWords);
+        ptx::cp_async16(&s.desc[st][lane], src + lane, P.pol);
+      }
     }
-    return d;
+    if (lane == 0) {
+      s.kind[st] = kind;
+      s.tile[st] = tile;
+    }
+    ptx::cp_async_commit();
   };
-  auto run_item = [&](int item, const Desc& d) {
-    int o = 0;
-    const int kind = classify(item, o);
-    if (kind == kLongChunk) return P.chunk_item(d, o % Tl, true);
-    if (kind == kShortChunk) return P.chunk_item(d, o % Ts, false);
-    return P.combine_task(d.w[0], o % Tc, Tl);
-  };
-  // Claims increase within a CTA.  Step k processes the item claimed at step k-3, whose
-  // entry was fetched at step k-2, fetches the entry of the item claimed at step k-1
-  // and claims a new one.  The three slots are unrolled so each keeps its own registers.
-  auto claim = [&]() {
-    int v = 0;
-    if (!kWarpCopy || (threadIdx.x & 31) == 0) v = G0 + atomicAdd(work, 1);
-    if (kWarpCopy) v = __shfl_sync(kFull, v, 0);
-    return v;
+  // Issues the item staged in `st`: 1 issued, 0 end of the work, -1 gave up.
+  auto issue = [&](int st) {
+    ptx::cp_async_wait<kStageAhead>();   // this lane's copies staged kStageAhead steps ago
+    __syncwarp();                        // ... and every other lane's
+    const int kind = s.kind[st], tile = s.tile[st];
+    if (kind == kEnd) return 0;
+    const int* d = reinterpret_cast<const int*>(&s.desc[st][0]);
+    bool ok;
+    if (kind == kCombine) ok = P.combine_task(d, tile, Tl);
+    else ok = P.chunk_item(d, tile, kind == kLongChunk);
+    return ok ? 1 : -1;
   };
 
-  int it[3];
-  Desc d[3];
-  it[0] = static_cast<int>(blockIdx.x) < G0 ? static_cast<int>(blockIdx.x) : claim();
-  it[1] = claim();
-  it[2] = claim();
-  d[0] = fetch(it[0]);
-  d[1] = fetch(it[1]);
+  // Step k stages the item claimed kClaimAhead steps earlier (lane 0 holds it in
+  // c[k % kClaimAhead]), claims the item it will stage kClaimAhead steps later into the
+  // same register, and issues the item staged kStageAhead steps earlier.  The loop over
+  // c is unrolled so each claim keeps its own register and is read only when it is due.
+  // Claims increase within a CTA; once one is past the end, so are the later ones.
+  int c[kClaimAhead];
+#pragma unroll
+  for (int j = 0; j < kClaimAhead; ++j) c[j] = total;
+  if (lane == 0) {
+    c[0] = static_cast<int>(blockIdx.x) < G0 ? static_cast<int>(blockIdx.x) : G0 + atomicAdd(work, 1);
+#pragma unroll
+    for (int j = 1; j < kClaimAhead; ++j) c[j] = G0 + atomicAdd(work, 1);
+  }
+  int k = 0;
   bool more = true;
   while (more) {
 #pragma unroll
-    for (int j = 0; j < 3; ++j) {
+    for (int j = 0; j < kClaimAhead; ++j) {
       if (more) {
-        d[(j + 2) % 3] = fetch(it[(j + 2) % 3]);
-        if (it[j] >= total || !P.ok) {
-          more = false;
-        } else {
-          P.ok = run_item(it[j], d[j]);
-          it[j] = claim();
+        const int v = __shfl_sync(kFull, c[j], 0);
+        stage(v, k % kStage);
+        if (lane == 0) c[j] = v < total ? G0 + atomicAdd(work, 1) : total;
+        if (k >= kStageAhead) {
+          const int r = issue((k - kStageAhead) % kStage);
+          if (r <= 0) {
+            more = false;
+            P.ok = r == 0;
+          }
         }
+        ++k;
       }
     }
   }
+  ptx::cp_async_wait<0>();
   P.finish_stream();
 }
 
@@ -537,7 +527,7 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
   const int t = threadIdx.x;
   if (t == 0) {
     for (int i = 0; i < kSlots; ++i) {
-      ptx::mbar_init(&s.full[i], kFullArrivals);
+      ptx::mbar_init(&s.full[i], 1);
       ptx::mbar_init(&s.empty[i], kConsumerWarps);
     }
     ptx::fence_mbar_init();
@@ -584,7 +574,7 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
   __syncthreads();
 
   if (t >= kConsumers) {
-    if (kWarpCopy || t == kConsumers) produce<GBF16, MBF16>(a, s, ring);
+    produce<GBF16, MBF16>(a, s, ring);   // the whole producer warp
     return;
   }
   consume<GBF16, MBF16>(a, s, ring);

@@ -69,6 +69,16 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t 
                : "memory");
 }
 
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Waits until at most N of this thread's most recent cp.async groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 // Arrive on `bar` once every cp.async this thread has issued so far has landed; the
 // arrival is already counted in the barrier's expected count (.noinc).
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
