@@ -153,12 +153,19 @@ __device__ __forceinline__ void finish(const ApplyArgs& a, const float t[8],
   }
 }
 
-// Index of list element `ord` (ordinals increase along the calls) given the
-// per-partition prefix counts and offsets; `cur` is the partition cursor.
+// Index of list element `ord` (< the list's length) given the per-partition prefix
+// counts and offsets, found by the whole warp: the partition holding `ord` is the last
+// one whose prefix is at most `ord` (an empty partition shares its prefix with the
+// next, so it is never the last such one unless it is the last partition, which then
+// holds `ord`).
 __device__ __forceinline__ int list_index(const int* prefix, const int* offset, int parts, int ord,
-                                          int& cur) {
-  while (cur + 1 < parts && ord >= prefix[cur + 1]) ++cur;
-  return offset[cur] + (ord - prefix[cur]);
+                                          int lane) {
+  int n = 0;
+  for (int p0 = 0; p0 < parts; p0 += 32) {
+    const int p = p0 + lane;
+    n += __popc(__ballot_sync(kFull, p < parts && prefix[p] <= ord));
+  }
+  return offset[n - 1] + (ord - prefix[n - 1]);
 }
 
 // The producer warp of a CTA.  Its 32 lanes take the same steps in lockstep, so every
@@ -374,7 +381,6 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int S1 = (S - G0) / 2;
   const int total = L + S + F;
   int* work = const_cast<int*>(&a.header->work[0]);
-  int cur0 = 0, cur1 = 0, cur2 = 0;   // list cursors (ordinals increase along the claims)
 
   // Stages the table entry of `item` (its chunk descriptor, or its long-run row) in
   // shared-memory stage `st` with asynchronous copies (one commit group per lane and
@@ -393,9 +399,7 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
       const int T = list == 0 ? Tl : list == 1 ? Ts : Tc;
       const int e = o / T;
       tile = o - e * T;
-      const int idx = list == 0   ? list_index(s.prefix[0], s.offset[0], parts, e, cur0)
-                      : list == 1 ? list_index(s.prefix[1], s.offset[1], parts, e, cur1)
-                                  : list_index(s.prefix[2], s.offset[2], parts, e, cur2);
+      const int idx = list_index(s.prefix[list], s.offset[list], parts, e, lane);
       if (kind == kCombine) {
         if (lane == 0) ptx::cp_async16(&s.desc[st][0], reinterpret_cast<const int4*>(a.runs) + idx, P.pol);
       } else if (lane < kChunkWords / 4) {
