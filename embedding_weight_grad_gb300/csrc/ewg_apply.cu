@@ -362,43 +362,54 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int Ts = (a.hidden + a.tile_cols_rest - 1) / a.tile_cols_rest;
   const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
   // Work items, in the order they are handed out (counts fit in 32 bits, checked on the
-  // host).  The first G0 = min(G, short items) are the static first items of CTAs
-  // 0..G0-1; every other item is claimed from the kernel's counter, so a CTA owns a
-  // long-run chunk only once it is running.  A fold waits only for chunks handed out
-  // before it, each owned by a running CTA that processes its items in claim order and
-  // never waits on a chunk item: the waits end whether or not all CTAs are resident.
-  //   [0, G0)                short-run chunk items (static)
-  //   [G0, G0+L)             chunks of long runs, each over a column tile -> partial rows
-  //   [G0+L, G0+L+S1)        half of the other short-run chunk items
+  // host).  A "unit" is one short-run chunk over all its column tiles (one claim, one
+  // descriptor, Ts tile copies); a "tile item" is one chunk over one column tile; a
+  // fold is one (long run, 512-column group).  The first G0 = min(G, short chunks)
+  // items are the static first items of CTAs 0..G0-1; every other item is claimed from
+  // the kernel's counter, so a CTA owns a long-run chunk only once it is running.  A
+  // fold waits only for chunks handed out before it, each owned by a running CTA that
+  // processes its items in claim order and never waits on a chunk item: the waits end
+  // whether or not all CTAs are resident.  The last short chunks go out as tile items,
+  // so the work ends in small pieces.
+  //   [0, G0)                units: short chunks 0..G0-1 (static)
+  //   [G0, G0+L)             tile items of the long runs' chunks -> partial rows
+  //   [G0+L, G0+L+S1)        units: short chunks G0..G0+S1-1
   //   [G0+L+S1, G0+L+S1+F)   folds of the long runs (their partial rows are mostly done
   //                          by then; a fold waits for the rest on the run's counter)
-  //   [G0+L+S1+F, L+S+F)     the remaining short-run chunk items
+  //   [G0+L+S1+F, total)     tile items of the remaining short chunks
   const int L = s.prefix[0][parts] * Tl;
-  const int S = s.prefix[1][parts] * Ts;
+  const int S = s.prefix[1][parts];   // short chunks
   const int F = s.prefix[2][parts] * Tc;
   const int G = static_cast<int>(gridDim.x);
   const int G0 = min(G, S);
   const int S1 = (S - G0) / 2;
-  const int total = L + S + F;
+  const int R0 = G0 + L + S1 + F;     // first tile item of the remaining short chunks
+  const int total = R0 + (S - G0 - S1) * Ts;
   int* work = const_cast<int*>(&a.header->work[0]);
 
   // Stages the table entry of `item` (its chunk descriptor, or its long-run row) in
   // shared-memory stage `st` with asynchronous copies (one commit group per lane and
-  // call), and records the item's kind and column tile (or fold group).
+  // call), and records the item's kind and column tile (fold: column group; unit: -1).
   auto stage = [&](int item, int st) {
     __syncwarp();   // every lane's reads of this stage's previous entry are done
-    int kind = kEnd, tile = 0;
+    int kind = kEnd, tile = -1;
     if (item < total) {
-      int o;
-      if (item < G0) { kind = kShortChunk; o = item; }
-      else if (item < G0 + L) { kind = kLongChunk; o = item - G0; }
-      else if (item < G0 + L + S1) { kind = kShortChunk; o = item - L; }
-      else if (item < G0 + L + S1 + F) { kind = kCombine; o = item - G0 - L - S1; }
-      else { kind = kShortChunk; o = item - L - F; }
-      const int list = kind == kLongChunk ? 0 : kind == kShortChunk ? 1 : 2;
-      const int T = list == 0 ? Tl : list == 1 ? Ts : Tc;
-      const int e = o / T;
-      tile = o - e * T;
+      int list, e;
+      if (item < G0) {
+        kind = kShortChunk, list = 1, e = item;
+      } else if (item < G0 + L) {
+        kind = kLongChunk, list = 0, e = (item - G0) / Tl;
+        tile = item - G0 - e * Tl;
+      } else if (item < G0 + L + S1) {
+        kind = kShortChunk, list = 1, e = item - L;
+      } else if (item < R0) {
+        kind = kCombine, list = 2, e = (item - G0 - L - S1) / Tc;
+        tile = item - G0 - L - S1 - e * Tc;
+      } else {
+        const int o = item - R0, q = o / Ts;
+        kind = kShortChunk, list = 1, e = G0 + S1 + q;
+        tile = o - q * Ts;
+      }
       const int idx = list_index(s.prefix[list], s.offset[list], parts, e, lane);
       if (kind == kCombine) {
         if (lane == 0) ptx::cp_async16(&s.desc[st][0], reinterpret_cast<const int4*>(a.runs) + idx, P.pol);
@@ -420,9 +431,14 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
     const int kind = s.kind[st], tile = s.tile[st];
     if (kind == kEnd) return 0;
     const int* d = reinterpret_cast<const int*>(&s.desc[st][0]);
-    bool ok;
-    if (kind == kCombine) ok = P.combine_task(d, tile, Tl);
-    else ok = P.chunk_item(d, tile, kind == kLongChunk);
+    bool ok = true;
+    if (kind == kCombine) {
+      ok = P.combine_task(d, tile, Tl);
+    } else if (tile >= 0) {
+      ok = P.chunk_item(d, tile, kind == kLongChunk);
+    } else {   // a unit: every column tile of the short chunk
+      for (int tt = 0; tt < Ts && ok; ++tt) ok = P.chunk_item(d, tt, false);
+    }
     return ok ? 1 : -1;
   };
 
