@@ -38,9 +38,10 @@ enum ItemKind { kEnd = -1, kShortChunk = 0, kLongChunk = 1, kCombine = 2 };
 // The producer's lookahead: an item is claimed kClaimAhead steps before its table entry
 // is staged in shared memory, and staged kStageAhead steps before it is issued, so
 // neither the claim (an atomic on a counter all CTAs share) nor the entry's load stalls
-// the issue.
-constexpr int kClaimAhead = 3;
-constexpr int kStageAhead = 2;
+// the issue.  Deeper lookahead was measured to lengthen the end of the kernel: a CTA
+// holding claimed items finishes late while others have run dry.
+constexpr int kClaimAhead = 2;
+constexpr int kStageAhead = 1;
 constexpr int kStage = kStageAhead + 1;   // staged entries: in flight + the one issued
 
 struct Item {
