@@ -61,6 +61,16 @@ def dist_env():
     return world, rank, local
 
 
+def reduce_max(values, world, device):
+    """Element-wise maximum of `values` over the ranks (one all_reduce; the identity on
+    one rank).  Every rank runs its own replica, so the job takes as long as its slowest
+    rank."""
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -294,15 +304,13 @@ def run_ours(args, w, world, rank, local):
     sampler.mark()
     sampler.stop()
 
-    t = torch.tensor([statistics.fmean(per_call)], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    mean_ms = float(t.item())
+    mean_ms, median_ms, plan_mean, apply_mean, e2e_mean = reduce_max(
+        [statistics.fmean(per_call), statistics.median(per_call), statistics.fmean(plan_ms),
+         statistics.fmean(apply_ms), statistics.fmean(e2e_ms)], world, dev)
 
     out = None
     if rank == 0:
         hbm_peak, peak_kind = peaks()
-        apply_mean = statistics.fmean(apply_ms)
         achieved = apply_bytes / (apply_mean * 1e-3) / 1e9
         traffic = traffic_from_profile(kernel_source_hash())
         launches_per_call = kernel_launches_per_call(n, V)
@@ -328,11 +336,12 @@ def run_ours(args, w, world, rank, local):
                 "unique_ids": U, "l2": "256 MiB memset before every timed call",
                 "parallelism": f"replicas x{world}",
             },
-            "median_us": round(statistics.median(per_call) * 1e3, 3),
+            "median_us": round(median_ms * 1e3, 3),
             "hbm_gbs": round(call_bytes / (mean_ms * 1e-3) / 1e9, 1),
+            "job_hbm_gbs": round(world * call_bytes / (mean_ms * 1e-3) / 1e9, 1),
             "frac_of_8tbs": round(call_bytes / (mean_ms * 1e-3) / 8e12, 4),
             "algorithmic_bytes_per_call": call_bytes,
-            "plan_us": round(statistics.fmean(plan_ms) * 1e3, 3),
+            "plan_us": round(plan_mean * 1e3, 3),
             "apply_us": round(apply_mean * 1e3, 3),
             "roofline": {
                 "kernel": "apply_kernel (one ewg_apply call)",
@@ -343,7 +352,7 @@ def run_ours(args, w, world, rank, local):
                 "traffic": traffic,
             },
             "e2e": {
-                "value": round(statistics.fmean(e2e_ms) * 1e3, 3), "unit": "us/call",
+                "value": round(e2e_mean * 1e3, 3), "unit": "us/call",
                 "h2d_bytes_per_step": ids_h.nbytes + grad_h.numel() * grad_h.element_size(),
                 "d2h_bytes_per_step": 4,
             },
