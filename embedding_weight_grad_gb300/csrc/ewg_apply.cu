@@ -44,6 +44,18 @@ constexpr int kClaimAhead = 2;
 constexpr int kStageAhead = 1;
 constexpr int kStage = kStageAhead + 1;   // staged entries: in flight + the one issued
 
+// Short chunks of at most kWideRows rows, handed out as whole-row units, are copied in
+// tiles twice as wide: half as many items to issue and consume for the same bytes.
+constexpr int kWideRows = 2;
+// Every item fits the ring: a 10-row chunk over the widest tile (with its main_grad
+// segment), a wide tile of kWideRows rows, a fold batch.
+static_assert(kNrows * kMaxTileColsBf16 * 2 + kMaxTileColsBf16 * 4 <= kRingBytes &&
+                  kNrows * kMaxTileColsFp32 * 4 + kMaxTileColsFp32 * 4 <= kRingBytes &&
+                  kWideRows * 2 * kMaxTileColsBf16 * 2 + 2 * kMaxTileColsBf16 * 4 <= kRingBytes &&
+                  kWideRows * 2 * kMaxTileColsFp32 * 4 + 2 * kMaxTileColsFp32 * 4 <= kRingBytes &&
+                  kCombineBatch * kCombineCols * 4 + kCombineCols * 4 <= kRingBytes,
+              "every ring item fits the ring");
+
 struct Item {
   int off;        // byte offset of the item in the ring
   int rows;       // grad rows (chunks) or partial rows (combine) in the ring
@@ -236,8 +248,7 @@ struct Producer {
 
   // One (chunk, column tile) item: the chunk's grad row segments (lane k: row k), plus
   // the main_grad segment (lane len) when the run has no other chunk.
-  __device__ bool chunk_item(const int* d, int tile, bool is_long) {
-    const int tc = is_long ? a.tile_cols_long : a.tile_cols_rest;
+  __device__ bool chunk_item(const int* d, int tile, int tc, bool is_long) {
     const int col0 = tile * tc;
     const int cols = min(tc, a.hidden - col0);
     const int meta = d[kDescMeta];
@@ -293,20 +304,24 @@ struct Producer {
     return true;
   }
 
-  // One (long run, 512-column group) fold, as batches of partial rows (lane k: row k of
-  // the batch); the last batch also brings the main_grad segment.
+  // One fold: a column slice (the whole 512-column group, or the entry's 1/split of it)
+  // of a long run, as batches of partial rows (lane k: row k of the batch); the last
+  // batch also brings the main_grad segment.
   __device__ bool combine_task(const int* run, int group, int Tl) {
     const int prow0 = run[0], C = run[1], id = run[2];
+    const int split = run[3] >> 4, width = kCombineCols / split;
+    const int col0 = group * kCombineCols + (run[3] & 15) * width;
+    const int cols = min(width, a.hidden - col0);
+    if (cols <= 0) return true;   // a slice past the last column: nothing to fold
     if (!wait_run(prow0, (s.epoch + 1) * C * Tl * kConsumerWarps)) {
       if (lane == 0) give_up(a, &s.abort);
       return false;
     }
-    const int col0 = group * kCombineCols;
-    const int cols = min(kCombineCols, a.hidden - col0);
     const uint32_t row_bytes = cols * 4;
     const uint32_t mg_bytes = cols * (MBF16 ? 2 : 4);
-    for (int b0 = 0; b0 < C; b0 += kCombineBatch) {
-      const int nb = min(kCombineBatch, C - b0);
+    const int batch = min(kCombineBatch * split, 31);   // about 16 KB of partial rows
+    for (int b0 = 0; b0 < C; b0 += batch) {
+      const int nb = min(batch, C - b0);
       const bool last = b0 + nb == C;
       const uint32_t bytes = nb * row_bytes + (last ? mg_bytes : 0u);
       const int off = reserve(bytes);
@@ -362,6 +377,9 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   const int Tl = (a.hidden + a.tile_cols_long - 1) / a.tile_cols_long;
   const int Ts = (a.hidden + a.tile_cols_rest - 1) / a.tile_cols_rest;
   const int Tc = (a.hidden + kCombineCols - 1) / kCombineCols;
+  // wide tiles: half as many as Ts, for units of at most kWideRows rows
+  const int Tw = (Ts + 1) / 2;
+  const int tcw = ((a.hidden + Tw - 1) / Tw + 7) / 8 * 8;
   // Work items, in the order they are handed out (counts fit in 32 bits, checked on the
   // host).  A "unit" is one short-run chunk over all its column tiles (one claim, one
   // descriptor, Ts tile copies); a "tile item" is one chunk over one column tile; a
@@ -436,9 +454,12 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
     if (kind == kCombine) {
       ok = P.combine_task(d, tile, Tl);
     } else if (tile >= 0) {
-      ok = P.chunk_item(d, tile, kind == kLongChunk);
-    } else {   // a unit: every column tile of the short chunk
-      for (int tt = 0; tt < Ts && ok; ++tt) ok = P.chunk_item(d, tt, false);
+      ok = P.chunk_item(d, tile, kind == kLongChunk ? a.tile_cols_long : a.tile_cols_rest,
+                        kind == kLongChunk);
+    } else {   // a unit: every column tile of the short chunk; few rows take wide tiles
+      const bool wide = (d[kDescMeta] & 15) <= kWideRows;
+      const int tc = wide ? tcw : a.tile_cols_rest, T = wide ? Tw : Ts;
+      for (int tt = 0; tt < T && ok; ++tt) ok = P.chunk_item(d, tt, tc, false);
     }
     return ok ? 1 : -1;
   };

@@ -35,8 +35,15 @@ constexpr int kDescMeta = 11;        // len | (c << 4), c = chunk index within t
 constexpr int kDescPartial = 12;     // partial row of this chunk (long runs), else -1
 constexpr int kDescNumChunks = 13;   // C, chunks of the run
 
-// Long-run table entry: 4 x int32.
-constexpr int kRunWords = 4;         // first partial row, C, id, unused
+// Long-run table entry: 4 x int32: first partial row, C, id, q | (split << 4).  A run of
+// many chunks is listed `split` times (q = 0..split-1); entry q folds the q-th of
+// `split` equal column slices of every 512-column group, so the long folds of heavy runs
+// spread over several CTAs.
+constexpr int kRunWords = 4;
+
+__host__ __device__ inline int fold_entries(int chunks) {
+  return chunks > 64 ? 4 : chunks > 32 ? 2 : 1;
+}
 
 // Partition tables: kTables arrays of kMaxParts ints.
 constexpr int kMaxParts = 128;
@@ -102,7 +109,10 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Long runs of L >= 11 rows have ceil(L/10) <= 2L/11 chunks; partition b of the hashed
 // plan starts its partial rows at floor(2 S_b / 11) + b (S_b: tokens of partitions < b).
 inline int64_t max_partial_rows(int64_t n) { return 2 * n / 11 + kMaxParts + 1; }
-inline int64_t max_long_runs(int64_t n) { return n / 11 + kMaxParts + 1; }
+// Table entries: a run of L >= 11 rows has at most L/11 + L/100 of them (one per run, two
+// above 320 rows, four above 640); partition b of the hashed plan starts its entries at
+// floor(S_b / 11) + floor(S_b / 100) + b.
+inline int64_t max_long_runs(int64_t n) { return n / 11 + n / 100 + kMaxParts + 1; }
 
 struct Layout {
   size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, hist, tile_bad, tile_cnt, arrivals,

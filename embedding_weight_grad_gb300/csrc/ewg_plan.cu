@@ -214,7 +214,7 @@ struct Listing {
       if (s < n && (s - rs[i]) % kNrows == 0) {
         if (re[i] - rs[i] + 1 > kNrows) {
           c += 1ll << kField;
-          if (s == rs[i]) c += 1;
+          if (s == rs[i]) c += fold_entries((re[i] - rs[i] + kNrows) / kNrows);
         } else {
           c += 1ll << (2 * kField);
         }
@@ -250,9 +250,12 @@ struct Listing {
       d[3] = make_int4(prow, C, 0, 0);
       if (is_long) {
         if (c == 0) {
-          reinterpret_cast<int4*>(a.runs)[b.run + ri] = make_int4(prow, C, static_cast<int>(key[i]), 0);
+          const int split = fold_entries(C);
+          for (int q = 0; q < split; ++q)
+            reinterpret_cast<int4*>(a.runs)[b.run + ri + q] =
+                make_int4(prow, C, static_cast<int>(key[i]), q | (split << 4));
           a.arrivals[prow] = 0;
-          ++ri;
+          ri += split;
         }
         ++li;
       } else {
@@ -456,7 +459,8 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   for (int s = t; s < TS; s += kHashThreads) {
     const int L = static_cast<int>(tcnt[s]);
     if (L > kNrows) {
-      cnt += (static_cast<long long>((L + kNrows - 1) / kNrows) << kField) + 1;
+      const int C = (L + kNrows - 1) / kNrows;
+      cnt += (static_cast<long long>(C) << kField) + fold_entries(C);
     } else if (L > 0) {
       cnt += 1ll << (2 * kField);
     }
@@ -465,7 +469,7 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   const long long pre = block_exclusive_scan<kHashThreads, long long>(cnt, SumOp(), 0ll, sw64, &tot);
   const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
   const int long_desc = S_b, short_desc = S_b + n_long;
-  const int partial_base = (2 * S_b) / 11 + part, run_base = S_b / 11 + part;
+  const int partial_base = (2 * S_b) / 11 + part, run_base = S_b / 11 + S_b / 100 + part;
   {
     int li = field_long(pre), si = field_short(pre), ri = field_runs(pre);
     for (int s = t; s < TS; s += kHashThreads) {
@@ -473,11 +477,13 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
       if (L > kNrows) {
         const int C = (L + kNrows - 1) / kNrows;
         tbase[s] = static_cast<uint32_t>(long_desc + li);
-        reinterpret_cast<int4*>(a.runs)[run_base + ri] =
-            make_int4(partial_base + li, C, static_cast<int>(tkey[s]), 0);
+        const int split = fold_entries(C);
+        for (int q = 0; q < split; ++q)
+          reinterpret_cast<int4*>(a.runs)[run_base + ri + q] =
+              make_int4(partial_base + li, C, static_cast<int>(tkey[s]), q | (split << 4));
         a.arrivals[partial_base + li] = 0;
         li += C;
-        ++ri;
+        ri += split;
       } else if (L > 0) {
         tbase[s] = static_cast<uint32_t>(short_desc + si);
         ++si;
