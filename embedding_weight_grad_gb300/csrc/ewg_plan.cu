@@ -322,6 +322,7 @@ constexpr size_t kHashSmem =
 // every run its descriptors, every key writes its own position word.
 
 __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a) {
+  ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
   extern __shared__ __align__(16) uint32_t sm[];
   uint32_t* kpos = sm;                   // position of key i (keys in position order)
@@ -528,6 +529,8 @@ __global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
   const int t = threadIdx.x, tile = blockIdx.x;
   const int B = a.passes ? 1 << min(a.digit_bits, a.id_bits) : 0;
   for (int i = t; i < B; i += kTileThreads) h[i] = 0;
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
   __syncthreads();
   int bad = 0;
   long long raw[kTileItems];
@@ -566,6 +569,8 @@ __global__ void __launch_bounds__(kTileThreads) hist_kernel(PlanArgs a, const ui
   const int sh = pass * a.digit_bits;
   const int B = 1 << min(a.digit_bits, a.id_bits - sh);
   for (int i = t; i < B; i += kTileThreads) h[i] = 0;
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
   __syncthreads();
   for (int r = 0; r < kTileItems; ++r) {
     const uint32_t k = keys[tile * kTile + r * kTileThreads + t];
@@ -576,30 +581,65 @@ __global__ void __launch_bounds__(kTileThreads) hist_kernel(PlanArgs a, const ui
 }
 
 // Exclusive scan of hist[bucket][tile] in (bucket, tile) order: each (bucket, tile)
-// gets the first output slot of its keys.
+// gets the first output slot of its keys.  Rounds of 16 entries per thread: each thread
+// loads its 16 consecutive entries at once, the block scans the per-thread sums, and a
+// carry links the rounds.
 __global__ void __launch_bounds__(1024) scan_hist_kernel(PlanArgs a, int pass) {
+  constexpr int IT = 16;
   __shared__ long long sw64[32];
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
   const int t = threadIdx.x;
   const int sh = pass * a.digit_bits;
   const long long E = static_cast<long long>(1 << min(a.digit_bits, a.id_bits - sh)) * a.tiles;
-  const long long per = (E + 1023) / 1024;
-  const long long b0 = min(E, t * per), b1 = min(E, b0 + per);
-  long long local = 0;
-  for (long long i = b0; i < b1; ++i) local += a.hist[i];
-  long long run = block_exclusive_scan<1024, long long>(local, SumOp(), 0ll, sw64, nullptr);
-  for (long long i = b0; i < b1; ++i) {
-    const uint32_t c = a.hist[i];
-    a.hist[i] = static_cast<uint32_t>(run);
-    run += c;
+  long long carry = 0;
+  for (long long base = 0; base < E; base += 1024 * IT) {
+    const long long i0 = base + static_cast<long long>(t) * IT;
+    uint32_t v[IT];
+    if (i0 + IT <= E) {   // 64-byte aligned: the region is 256-byte aligned, i0 % 16 == 0
+      const uint4* src = reinterpret_cast<const uint4*>(a.hist + i0);
+#pragma unroll
+      for (int q = 0; q < IT / 4; ++q) {
+        const uint4 x = src[q];
+        v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < IT; ++k) v[k] = i0 + k < E ? a.hist[i0 + k] : 0u;
+    }
+    long long local = 0;
+#pragma unroll
+    for (int k = 0; k < IT; ++k) local += v[k];
+    long long round_total = 0;
+    long long run = carry + block_exclusive_scan<1024, long long>(local, SumOp(), 0ll, sw64,
+                                                                  &round_total);
+#pragma unroll
+    for (int k = 0; k < IT; ++k) {
+      const uint32_t c = v[k];
+      v[k] = static_cast<uint32_t>(run);
+      run += c;
+    }
+    if (i0 + IT <= E) {
+      uint4* dst = reinterpret_cast<uint4*>(a.hist + i0);
+#pragma unroll
+      for (int q = 0; q < IT / 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < IT; ++k)
+        if (i0 + k < E) a.hist[i0 + k] = v[k];
+    }
+    carry += round_total;
   }
 }
 
-// Stable scatter of one tile for one pass.
+// Stable scatter of one tile for one pass.  Every global load of the tile (keys,
+// positions, the tile's output bases of this thread's digits) is issued up front.
 __global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const uint32_t* ks,
                                                                const uint32_t* vs, uint32_t* kd,
                                                                uint32_t* vd, int pass) {
   constexpr int NW = kTileThreads / 32;
   constexpr int kStride = 1 << kMaxDigitBits;
+  constexpr int kDigitsPerThread = kStride / kTileThreads;
   __shared__ uint32_t cnt[NW * kStride];   // [warp][bucket]
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, tile = blockIdx.x;
   const int sh = pass * a.digit_bits;
@@ -607,12 +647,25 @@ __global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const
   const uint32_t lt = (1u << lane) - 1u;
   for (int w = 0; w < NW; ++w)
     for (uint32_t d = t; d < B; d += kTileThreads) cnt[w * kStride + d] = 0;
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
+  uint32_t key[kTileItems], val[kTileItems], hb[kDigitsPerThread];
+#pragma unroll
+  for (int r = 0; r < kTileItems; ++r) {
+    const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
+    key[r] = ks[idx];
+    val[r] = vs[idx];
+  }
+#pragma unroll
+  for (int j = 0; j < kDigitsPerThread; ++j) {
+    const uint32_t d = t + j * kTileThreads;
+    hb[j] = d < B ? a.hist[static_cast<long long>(d) * a.tiles + tile] : 0u;
+  }
   __syncthreads();
   uint32_t rank[kTileItems], dig[kTileItems];
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
-    const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
-    const uint32_t d = (ks[idx] >> sh) & mask;
+    const uint32_t d = (key[r] >> sh) & mask;
     const unsigned peers = __match_any_sync(kFull, d);
     const uint32_t prior = cnt[warp * kStride + d];
     __syncwarp();
@@ -622,35 +675,63 @@ __global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const
     dig[r] = d;
   }
   __syncthreads();
-  for (uint32_t d = t; d < B; d += kTileThreads) {
-    uint32_t run = a.hist[static_cast<long long>(d) * a.tiles + tile];
-    for (int w = 0; w < NW; ++w) {
-      const uint32_t c = cnt[w * kStride + d];
-      cnt[w * kStride + d] = run;
-      run += c;
+#pragma unroll
+  for (int j = 0; j < kDigitsPerThread; ++j) {
+    const uint32_t d = t + j * kTileThreads;
+    if (d < B) {
+      uint32_t run = hb[j];
+      for (int w = 0; w < NW; ++w) {
+        const uint32_t c = cnt[w * kStride + d];
+        cnt[w * kStride + d] = run;
+        run += c;
+      }
     }
   }
   __syncthreads();
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
-    const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
     const uint32_t dst = cnt[warp * kStride + dig[r]] + rank[r];
-    kd[dst] = ks[idx];
-    vd[dst] = vs[idx];
+    kd[dst] = key[r];
+    vd[dst] = val[r];
   }
 }
 
-// Run bounds of the slots at the two ends of a tile, found by warp 0.
+// Bound of key k, like warp_bound, looking first at the 32 slots next to `at` (the
+// start of the search for an upper bound, the end for a lower bound): most runs are
+// short, so one load usually settles it.
+__device__ int warp_bound_near(const uint32_t* keys, int lo, int hi, int at, uint32_t k, bool upper) {
+  const int lane = threadIdx.x & 31;
+  if (upper) {   // first index in [at, hi) with key > k
+    const int w1 = min(hi, at + 32);
+    const int idx = at + lane;
+    const bool pred = idx < w1 ? keys[idx] > k : true;
+    const unsigned m = __ballot_sync(kFull, pred);
+    const int f = __ffs(m) - 1;   // -1 when all 32 slots of a full window hold k
+    if (m != 0 && (at + f < w1 || w1 == hi)) return min(at + f, hi);
+    return warp_bound(keys, w1, hi, k, true);
+  }
+  // first index in [lo, at + 1) with key >= k
+  const int w0 = max(lo, at - 31);
+  const int idx = w0 + lane;
+  const bool pred = idx <= at ? keys[idx] >= k : true;
+  const unsigned m = __ballot_sync(kFull, pred);
+  const int f = __ffs(m) - 1;     // m != 0: slot `at` holds k
+  if (f > 0 || w0 == lo) return w0 + f;
+  return warp_bound(keys, lo, w0 + 1, k, false);
+}
+
+// Run bounds of the slots at the two ends of a tile: warp 0 finds where the run of the
+// first slot starts, warp 1 where the run of the last slot ends.
 __device__ void tile_seeds(const uint32_t* keys, int n, int s0, int* rs_seed, int* re_seed) {
   __shared__ int seeds[2];
-  if (threadIdx.x < 32) {
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    const int rs = warp_bound_near(keys, 0, s0 + 1, s0, keys[s0], false);
+    if (threadIdx.x == 0) seeds[0] = rs;
+  } else if (warp == 1) {
     const int s1 = min(n, s0 + kTile) - 1;
-    const int rs = warp_bound(keys, 0, s0 + 1, keys[s0], false);
-    const int re = warp_bound(keys, s1, n, keys[s1], true) - 1;
-    if (threadIdx.x == 0) {
-      seeds[0] = rs;
-      seeds[1] = re;
-    }
+    const int re = warp_bound_near(keys, s1, n, s1, keys[s1], true) - 1;
+    if (threadIdx.x == 32) seeds[1] = re;
   }
   __syncthreads();
   *rs_seed = seeds[0];
@@ -661,9 +742,15 @@ __global__ void __launch_bounds__(kTileThreads) list_count_kernel(PlanArgs a,
                                                                   const uint32_t* keys) {
   __shared__ int swi[kTileThreads / 32];
   __shared__ long long sw64[kTileThreads / 32];
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
   const int s0 = blockIdx.x * kTile;
   int rs_seed, re_seed;
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
+  if (threadIdx.x == 0) {   // the sort is done with the histograms: keep the seeds there
+    a.hist[2 * blockIdx.x] = static_cast<uint32_t>(rs_seed);
+    a.hist[2 * blockIdx.x + 1] = static_cast<uint32_t>(re_seed);
+  }
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
   const long long tot = block_sum<kTileThreads>(L.counts(a.n, s0), sw64);
@@ -675,6 +762,8 @@ __global__ void __launch_bounds__(kTileThreads) list_count_kernel(PlanArgs a,
 // (single-partition) tables.
 __global__ void __launch_bounds__(1024) list_scan_kernel(PlanArgs a) {
   __shared__ long long sw64[32];
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
   const int t = threadIdx.x;
   const int per = (a.tiles + 1023) / 1024;
   const int b0 = min(a.tiles, t * per), b1 = min(a.tiles, b0 + per);
@@ -707,13 +796,14 @@ __global__ void __launch_bounds__(1024) list_scan_kernel(PlanArgs a) {
 
 __global__ void __launch_bounds__(kTileThreads) list_emit_kernel(PlanArgs a, const uint32_t* keys,
                                                                  const uint32_t* vals) {
-  ptx::pdl_launch_dependents();
   __shared__ int swi[kTileThreads / 32];
   __shared__ long long sw64[kTileThreads / 32];
+  ptx::pdl_wait_prior_grid();
+  ptx::pdl_launch_dependents();
   if (a.header->status != EWG_OK) return;
   const int s0 = blockIdx.x * kTile;
-  int rs_seed, re_seed;
-  tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
+  const int rs_seed = static_cast<int>(a.hist[2 * blockIdx.x]);
+  const int re_seed = static_cast<int>(a.hist[2 * blockIdx.x + 1]);
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
   const long long prefix =
@@ -735,21 +825,41 @@ cudaError_t prepare_kernels() {
                               static_cast<int>(kHashSmem));
 }
 
+namespace {
+
+// Launches `kernel` chained to the stream's previous work by programmatic dependent
+// launch: it may start while its predecessor finishes, and waits for it (every plan
+// kernel calls griddepcontrol.wait before reading anything the predecessor wrote).
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+}  // namespace
+
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
-  if (a.n <= kHashMaxN) {
-    plan_hashed_kernel<<<kHashParts, kHashThreads, kHashSmem, stream>>>(a);
-    return cudaGetLastError();
-  }
+  if (a.n <= kHashMaxN) return launch_pdl(plan_hashed_kernel, kHashParts, kHashThreads, kHashSmem, stream, a);
   const int tiles = a.tiles;
-  pack_hist_kernel<<<tiles, kTileThreads, 0, stream>>>(a);
+  cudaError_t e = launch_pdl(pack_hist_kernel, tiles, kTileThreads, 0, stream, a);
   const uint32_t* ks = a.keys_a;
   const uint32_t* vs = a.vals_a;
   uint32_t* kd = a.keys_b;
   uint32_t* vd = a.vals_b;
-  for (int pass = 0; pass < a.passes; ++pass) {
-    if (pass > 0) hist_kernel<<<tiles, kTileThreads, 0, stream>>>(a, ks, pass);
-    scan_hist_kernel<<<1, 1024, 0, stream>>>(a, pass);
-    scatter_kernel<<<tiles, kTileThreads, 0, stream>>>(a, ks, vs, kd, vd, pass);
+  for (int pass = 0; pass < a.passes && e == cudaSuccess; ++pass) {
+    if (pass > 0) e = launch_pdl(hist_kernel, tiles, kTileThreads, 0, stream, a, ks, pass);
+    if (e == cudaSuccess) e = launch_pdl(scan_hist_kernel, 1, 1024, 0, stream, a, pass);
+    if (e == cudaSuccess) e = launch_pdl(scatter_kernel, tiles, kTileThreads, 0, stream, a, ks, vs, kd, vd, pass);
     const uint32_t* nk = kd;
     const uint32_t* nv = vd;
     kd = const_cast<uint32_t*>(ks);
@@ -757,10 +867,10 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
     ks = nk;
     vs = nv;
   }
-  list_count_kernel<<<tiles, kTileThreads, 0, stream>>>(a, ks);
-  list_scan_kernel<<<1, 1024, 0, stream>>>(a);
-  list_emit_kernel<<<tiles, kTileThreads, 0, stream>>>(a, ks, vs);
-  return cudaGetLastError();
+  if (e == cudaSuccess) e = launch_pdl(list_count_kernel, tiles, kTileThreads, 0, stream, a, ks);
+  if (e == cudaSuccess) e = launch_pdl(list_scan_kernel, 1, 1024, 0, stream, a);
+  if (e == cudaSuccess) e = launch_pdl(list_emit_kernel, tiles, kTileThreads, 0, stream, a, ks, vs);
+  return e;
 }
 
 }  // namespace ewg
