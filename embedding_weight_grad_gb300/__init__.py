@@ -22,7 +22,7 @@ import torch
 __all__ = [
     "MIN_TOKENS", "MAX_TOKENS", "NROWS", "EwgError", "can_accumulate_embedding_wgrad",
     "accumulate_embedding_wgrad", "workspace_bytes", "plan", "apply", "read_status",
-    "library_path", "lib",
+    "library_path", "lib", "accumulate_embedding_wgrad_shard",
 ]
 
 MIN_TOKENS = 3073
@@ -72,6 +72,11 @@ def lib():
             L.ewg_plan.restype = i32
             L.ewg_apply.argtypes = [vp, i32, i64, vp, i32, i64, i64, i64, i64, vp, sz, vp]
             L.ewg_apply.restype = i32
+            L.ewg_accumulate_shard.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64,
+                                               i64, i64, vp, sz, vp]
+            L.ewg_accumulate_shard.restype = i32
+            L.ewg_plan_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, sz, vp]
+            L.ewg_plan_shard.restype = i32
             L.ewg_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
             L.ewg_read_status.restype = i32
             L.ewg_status_string.argtypes = [i32]
@@ -187,6 +192,32 @@ def accumulate_embedding_wgrad(ids: torch.Tensor, grad: torch.Tensor, main_grad:
         ws = workspace if workspace is not None else new_workspace(a.n, a.H, a.device)
         stream = _stream_ptr(a.device)
         _raise_on(L.ewg_accumulate(*a.c_args(), ws.data_ptr(), ws.numel(), stream))
+        if check:
+            raise_on_device_status(ws)
+
+
+def accumulate_embedding_wgrad_shard(ids: torch.Tensor, grad: torch.Tensor,
+                                     main_grad_shard: torch.Tensor, row_begin: int,
+                                     num_embeddings: int, *,
+                                     workspace: torch.Tensor | None = None,
+                                     check: bool = False) -> None:
+    """accumulate_embedding_wgrad restricted to the table rows
+    [row_begin, row_begin + main_grad_shard.shape[0]) of a num_embeddings-row table.
+
+    main_grad_shard holds those rows (its row 0 is table row row_begin) and ends with
+    the bits the whole-table call would give them; ids of other rows are skipped, ids
+    outside [0, num_embeddings) are errors.  One GPU per row range needs no exchange.
+    """
+    a = _Args(ids, grad, main_grad_shard)
+    if a.reason is not None:
+        raise ValueError(f"accumulate_embedding_wgrad_shard does not support these tensors: {a.reason}")
+    rows = a.V
+    with torch.cuda.device(a.device):
+        L = lib()
+        ws = workspace if workspace is not None else new_workspace(a.n, a.H, a.device)
+        args = list(a.c_args())
+        args[8:9] = [num_embeddings, row_begin, rows]   # V -> (num_embeddings, row_begin, rows)
+        _raise_on(L.ewg_accumulate_shard(*args, ws.data_ptr(), ws.numel(), _stream_ptr(a.device)))
         if check:
             raise_on_device_status(ws)
 

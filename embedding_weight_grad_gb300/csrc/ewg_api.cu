@@ -142,15 +142,22 @@ T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
 }
 
-int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t H, void* ws,
-            cudaStream_t stream) {
+// Rows [row_begin, row_begin + rows) of the [V, H] table are kept (the whole table:
+// row_begin = 0, rows = V).
+int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t row_begin,
+            int64_t rows, int64_t H, void* ws, cudaStream_t stream) {
   const ewg::Layout L = ewg::make_layout(n, H);
-  const ewg::SortPlan sp = ewg::make_sort_plan(V);
+  const bool sharded = row_begin != 0 || rows != V;
+  // a skipped id sorts as key `rows`, after the shard's own keys
+  const ewg::SortPlan sp = ewg::make_sort_plan(sharded ? rows : rows - 1);
   ewg::PlanArgs a{};
   a.ids = ids;
   a.ids_int64 = ids_dtype == EWG_INT64;
   a.n = static_cast<int>(n);
   a.num_embeddings = V;
+  a.row_begin = row_begin;
+  a.shard_rows = rows;
+  a.skip_key = sharded ? static_cast<uint32_t>(rows) : 0xffffffffu;
   a.hidden = static_cast<int>(H);
   a.id_bits = sp.id_bits;
   a.passes = sp.passes;
@@ -198,6 +205,12 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   return EWG_OK;
 }
 
+int check_shard(int64_t V, int64_t row_begin, int64_t rows) {
+  if (row_begin < 0 || rows < 1 || row_begin > V - rows)
+    return fail(EWG_ERR_UNSUPPORTED, "the shard [row_begin, row_begin + shard_rows) must lie in [0, num_embeddings)");
+  return EWG_OK;
+}
+
 }  // namespace
 
 void ewg::set_last_error(const char* msg) { g_last_error = msg; }
@@ -234,7 +247,7 @@ int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const voi
   if (rc) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace, s);
+  rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, 0, num_embeddings, hidden, workspace, s);
   if (rc) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
                   num_embeddings, hidden, main_grad_row_stride, workspace, sms, s);
@@ -249,7 +262,7 @@ int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_emb
   if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
   if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
-  return do_plan(ids, ids_dtype, num_tokens, num_embeddings, hidden, workspace,
+  return do_plan(ids, ids_dtype, num_tokens, num_embeddings, 0, num_embeddings, hidden, workspace,
                  static_cast<cudaStream_t>(stream));
 }
 
@@ -271,6 +284,44 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* m
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
                   num_embeddings, hidden, main_grad_row_stride, workspace, sms,
                   static_cast<cudaStream_t>(stream));
+}
+
+int ewg_accumulate_shard(const void* ids, int ids_dtype, int64_t num_tokens, const void* grad,
+                         int grad_dtype, int64_t grad_row_stride, void* main_grad,
+                         int main_grad_dtype, int64_t num_embeddings, int64_t row_begin,
+                         int64_t shard_rows, int64_t hidden, int64_t main_grad_row_stride,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  int dev = 0, sms = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
+  if ((rc = check_shard(num_embeddings, row_begin, shard_rows))) return rc;
+  // the shard's main_grad has shard_rows rows
+  rc = check_all(ids, ids_dtype, num_tokens, grad, grad_dtype, grad_row_stride, main_grad,
+                 main_grad_dtype, shard_rows, hidden, main_grad_row_stride, dev);
+  if (rc) return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, row_begin, shard_rows, hidden, workspace, s);
+  if (rc) return rc;
+  return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
+                  shard_rows, hidden, main_grad_row_stride, workspace, sms, s);
+}
+
+int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_embeddings,
+                   int64_t row_begin, int64_t shard_rows, int64_t hidden, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  g_last_error.clear();
+  int dev = 0, sms = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
+  if ((rc = check_shard(num_embeddings, row_begin, shard_rows))) return rc;
+  if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
+  if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  return do_plan(ids, ids_dtype, num_tokens, num_embeddings, row_begin, shard_rows, hidden,
+                 workspace, static_cast<cudaStream_t>(stream));
 }
 
 int ewg_read_status(const void* workspace, void* stream, int* status) {

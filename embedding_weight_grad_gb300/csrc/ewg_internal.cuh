@@ -166,9 +166,10 @@ inline int bit_width(uint64_t x) {
   return b;
 }
 
-inline SortPlan make_sort_plan(int64_t num_embeddings) {
+// Sort plan for keys in [0, max_key].
+inline SortPlan make_sort_plan(int64_t max_key) {
   SortPlan s{};
-  s.id_bits = bit_width(static_cast<uint64_t>(num_embeddings - 1));
+  s.id_bits = bit_width(static_cast<uint64_t>(max_key));
   s.passes = static_cast<int>(ceil_div(s.id_bits, kMaxDigitBits));
   s.digit_bits = s.passes ? static_cast<int>(ceil_div(s.id_bits, s.passes)) : 0;
   return s;
@@ -178,7 +179,10 @@ struct PlanArgs {
   const void* ids;
   int ids_int64;
   int n;
-  long long num_embeddings;
+  long long num_embeddings;   // ids outside [0, num_embeddings) are errors
+  long long row_begin;        // the rows kept: [row_begin, row_begin + shard_rows); an id
+  long long shard_rows;       // there becomes key id - row_begin, other ids are skipped
+  uint32_t skip_key;          // sort key of a skipped id (shard_rows when sharded)
   int hidden;
   int id_bits, passes, digit_bits;
   int tiles;

@@ -205,13 +205,13 @@ struct Listing {
     }
   }
 
-  __device__ long long counts(int n, int s_begin) const {
+  __device__ long long counts(int n, int s_begin, uint32_t skip_key) const {
     const int base = s_begin + threadIdx.x * ITEMS;
     long long c = 0;
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int s = base + i;
-      if (s < n && (s - rs[i]) % kNrows == 0) {
+      if (s < n && key[i] != skip_key && (s - rs[i]) % kNrows == 0) {
         if (re[i] - rs[i] + 1 > kNrows) {
           c += 1ll << kField;
           if (s == rs[i]) c += fold_entries((re[i] - rs[i] + kNrows) / kNrows);
@@ -232,7 +232,7 @@ struct Listing {
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int s = base + i;
-      if (s >= n || (s - rs[i]) % kNrows != 0) continue;
+      if (s >= n || key[i] == a.skip_key || (s - rs[i]) % kNrows != 0) continue;
       const int L = re[i] - rs[i] + 1;
       const int c = (s - rs[i]) / kNrows;
       const int len = min(kNrows, re[i] - s + 1);
@@ -269,7 +269,7 @@ __device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
   Header* h = a.header;
   h->n = a.n;
   h->hidden = a.hidden;
-  h->num_embeddings = a.num_embeddings;
+  h->num_embeddings = a.shard_rows;   // rows of the main_grad the apply may touch
   h->num_parts = num_parts;
   h->bad_ids = bad;
   h->work[0] = h->work[1] = 0;
@@ -356,12 +356,12 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
     if (p < a.n) {
       if (raw[r] < 0 || raw[r] >= a.num_embeddings) {
         ++bad;
-      } else {
-        key[r] = static_cast<uint32_t>(raw[r]);
+      } else if (raw[r] >= a.row_begin && raw[r] - a.row_begin < a.shard_rows) {
+        key[r] = static_cast<uint32_t>(raw[r] - a.row_begin);
+        const int h = hash_part(key[r]);
+        mine = h == part;
+        before += h < part;
       }
-      const int h = hash_part(key[r]);
-      mine = h == part;
-      before += h < part;
     }
     ballot[r] = __ballot_sync(kFull, mine);
     if (lane == 0) wc[r * kHashWarps + warp] = __popc(ballot[r]);
@@ -547,8 +547,10 @@ __global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
       if (raw[r] < 0 || raw[r] >= a.num_embeddings) {
         ++bad;
         k = 0u;
+      } else if (raw[r] >= a.row_begin && raw[r] - a.row_begin < a.shard_rows) {
+        k = static_cast<uint32_t>(raw[r] - a.row_begin);
       } else {
-        k = static_cast<uint32_t>(raw[r]);
+        k = a.skip_key;   // outside the shard: sorts after its rows, listed as nothing
       }
     }
     a.keys_a[i] = k;
@@ -753,7 +755,7 @@ __global__ void __launch_bounds__(kTileThreads) list_count_kernel(PlanArgs a,
   }
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
-  const long long tot = block_sum<kTileThreads>(L.counts(a.n, s0), sw64);
+  const long long tot = block_sum<kTileThreads>(L.counts(a.n, s0, a.skip_key), sw64);
   if (threadIdx.x == 0)
     a.tile_cnt[blockIdx.x] = make_int4(field_long(tot), field_short(tot), field_runs(tot), 0);
 }
@@ -807,7 +809,7 @@ __global__ void __launch_bounds__(kTileThreads) list_emit_kernel(PlanArgs a, con
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
   const long long prefix =
-      block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0), SumOp(), 0ll, sw64, nullptr);
+      block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0, a.skip_key), SumOp(), 0ll, sw64, nullptr);
   const int4 tp = a.tile_cnt[blockIdx.x];
   EmitBases eb;
   eb.long_desc = tp.x;

@@ -145,6 +145,43 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride,
               int64_t num_embeddings, int64_t hidden, int64_t main_grad_row_stride,
               void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Vocabulary-sharded ewg_accumulate: main_grad holds only the rows
+ * [row_begin, row_begin + shard_rows) of the [num_embeddings, hidden] table (its row 0 is
+ * table row row_begin), and the call updates exactly the rows of that range that
+ * ewg_accumulate would update, with the same bits.  Ids in [0, num_embeddings) outside
+ * the range are skipped; ids outside [0, num_embeddings) are errors as in
+ * ewg_accumulate.
+ *
+ * The page has no entry point of its own for this.  It follows from the module
+ * docstring of core.fusions.fused_embedding_wgrad: a row's result depends only on that
+ * token's own rows, in position order, and rows of absent tokens are not touched, so
+ * the rows of a range are computed the same way whatever happens to the other rows.
+ * One GPU per range of rows then needs no exchange.
+ *
+ * ids, grad: as in ewg_accumulate (all num_tokens tokens; the support condition on
+ * num_tokens is that of the whole call).  main_grad: shard_rows rows of hidden
+ * elements, row stride main_grad_row_stride.  Requires 0 <= row_begin,
+ * 1 <= shard_rows and row_begin + shard_rows <= num_embeddings (else
+ * EWG_ERR_UNSUPPORTED before anything is enqueued).  Workspace, stream and errors:
+ * as ewg_accumulate.
+ */
+int ewg_accumulate_shard(const void* ids, int ids_dtype, int64_t num_tokens,
+                         const void* grad, int grad_dtype, int64_t grad_row_stride,
+                         void* main_grad, int main_grad_dtype, int64_t num_embeddings,
+                         int64_t row_begin, int64_t shard_rows, int64_t hidden,
+                         int64_t main_grad_row_stride, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * The first half of ewg_accumulate_shard: ewg_plan keeping only the ids in
+ * [row_begin, row_begin + shard_rows), renumbered from 0.  The ewg_apply that follows
+ * takes num_embeddings = shard_rows and the shard's main_grad.
+ */
+int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens,
+                   int64_t num_embeddings, int64_t row_begin, int64_t shard_rows,
+                   int64_t hidden, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the library-owned scratch used by ewg_accumulate_static (64 MiB). */
 #define EWG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
