@@ -377,6 +377,30 @@ def run_ours(args, w, world, rank, local):
             out["clocks"] = clk
         if not args.no_extras:
             out["dense_path"] = dense_path(w, ids_d, grad_d, mg, args, stream, flush)
+            out["shards"] = shard_path(w, ids_d, grad_d, mg, args, stream, flush, ws)
+    return out
+
+
+def shard_path(w, ids_d, grad_d, mg, args, stream, flush, ws):
+    """The table split in two row halves, one ewg_accumulate_shard call each (on a
+    vocabulary-parallel setup each GPU runs one of them)."""
+    import embedding_weight_grad_gb300 as ewg
+
+    V = w.num_embeddings
+    half = V // 2
+    out = {}
+    for name, b0, b1 in (("rows_0_to_half", 0, half), ("rows_half_to_end", half, V)):
+        part = mg[b0:b1]
+
+        def call():
+            ewg.accumulate_embedding_wgrad_shard(ids_d, grad_d, part, b0, V, workspace=ws)
+
+        for _ in range(3):
+            flush()
+            call()
+        ms = time_events(call, 20, stream, flush)
+        out[name] = round(statistics.fmean(ms) * 1e3, 2)
+    out["unit"] = "us/call"
     return out
 
 
