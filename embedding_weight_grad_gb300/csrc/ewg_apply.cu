@@ -60,7 +60,7 @@ struct Item {
   int off;        // byte offset of the item in the ring
   int rows;       // grad rows (chunks) or partial rows (combine) in the ring
   int id;         // main_grad row
-  int prow;       // partial row to write (long chunk)
+  int prow;       // partial row to write (long chunk), first partial row read (fold)
   int col0;       // first column
   int cols;       // columns
   int kind;
@@ -326,7 +326,7 @@ struct Producer {
       const uint32_t bytes = nb * row_bytes + (last ? mg_bytes : 0u);
       const int off = reserve(bytes);
       if (off < 0) return false;
-      Item it{off, nb, id, -1, col0, cols, kCombine, (b0 == 0 ? 1 : 0) | (last ? 2 : 0)};
+      Item it{off, nb, id, prow0 + b0, col0, cols, kCombine, (b0 == 0 ? 1 : 0) | (last ? 2 : 0)};
       uint64_t* bar = open(it, bytes);
       if (lane < nb) {
         const float* src = a.partial + static_cast<long long>(prow0 + b0 + lane) * a.hidden + col0;
@@ -504,6 +504,7 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
 template <bool GBF16, bool MBF16>
 __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) {
   const int t = threadIdx.x, lane = t & 31;
+  const uint64_t pol_keep = ptx::policy_evict_last();
   float total[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) total[e] = 0.0f;
@@ -528,6 +529,12 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
         if (it.flags & 2)
           finish<GBF16, MBF16>(a, total, base + it.rows * row_bytes + c * (MBF16 ? 2 : 4), it.id,
                                it.col0 + c);
+        // The batch's partial rows are dead now: drop their L2 lines instead of writing
+        // them back.  Only when every fold slice is whole 128-byte lines (hidden % 32 == 0:
+        // rows and the 128-column slices then start on line boundaries).
+        if ((a.hidden & 31) == 0 && (c & 31) == 0)
+          for (int k = 0; k < it.rows; ++k)
+            ptx::discard_l2_line(a.partial + static_cast<long long>(it.prow + k) * a.hidden + it.col0 + c);
       }
     } else {   // chunk item: passes of 8 * kConsumers columns over the tile
       const uint32_t row_bytes = it.cols * (GBF16 ? 2 : 4);
@@ -538,10 +545,10 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
         for (int k = 0; k < it.rows; ++k)
           add_row<GBF16>(part, base + k * row_bytes + c * (GBF16 ? 2 : 4));
         if (it.kind == kLongChunk) {
-          float4* dst = reinterpret_cast<float4*>(a.partial + static_cast<long long>(it.prow) * a.hidden +
-                                                  it.col0 + c);
-          dst[0] = make_float4(part[0], part[1], part[2], part[3]);
-          dst[1] = make_float4(part[4], part[5], part[6], part[7]);
+          // partial rows are read back soon by the run's fold: ask L2 to keep them
+          float* dst = a.partial + static_cast<long long>(it.prow) * a.hidden + it.col0 + c;
+          ptx::st_global_v4(dst, part[0], part[1], part[2], part[3], pol_keep);
+          ptx::st_global_v4(dst + 4, part[4], part[5], part[6], part[7], pol_keep);
         } else {   // the run's only chunk: t = 0 + part
           float tt[8];
 #pragma unroll

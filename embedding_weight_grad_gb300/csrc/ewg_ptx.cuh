@@ -92,6 +92,20 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// 16-byte global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_v4(float* p, float a, float b, float c, float d,
+                                             uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(a),
+               "f"(b), "f"(c), "f"(d), "l"(policy)
+               : "memory");
+}
+
+// Drops a 128-byte L2 line (128-byte aligned) without writing it back: its contents
+// become undefined.  For data that is dead once read.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
