@@ -370,7 +370,7 @@ struct Producer {
 };
 
 template <bool GBF16, bool MBF16>
-__device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
+__device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring, int first_claim) {
   Producer<GBF16, MBF16> P(a, s, ring);
   const int lane = P.lane;
   const int parts = s.num_parts;
@@ -444,8 +444,11 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
     ptx::cp_async_commit();
   };
   // Issues the item staged in `st`: 1 issued, 0 end of the work, -1 gave up.
-  auto issue = [&](int st) {
-    ptx::cp_async_wait<kStageAhead>();   // this lane's copies staged kStageAhead steps ago
+  auto issue = [&](int st, bool newest) {
+    // this lane's copies for `st`: the newest group (nothing staged since), or the one
+    // staged kStageAhead steps ago
+    if (newest) ptx::cp_async_wait<0>();
+    else ptx::cp_async_wait<kStageAhead>();
     __syncwarp();                        // ... and every other lane's
     const int kind = s.kind[st], tile = s.tile[st];
     if (kind == kEnd) return 0;
@@ -472,10 +475,12 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
   int c[kClaimAhead];
 #pragma unroll
   for (int j = 0; j < kClaimAhead; ++j) c[j] = total;
-  if (lane == 0) {
-    c[0] = static_cast<int>(blockIdx.x) < G0 ? static_cast<int>(blockIdx.x) : G0 + atomicAdd(work, 1);
+  if (lane == 0) {   // first_claim: this CTA's first counter claim, made in the prologue
+    const bool fixed = static_cast<int>(blockIdx.x) < G0;
+    c[0] = fixed ? static_cast<int>(blockIdx.x) : G0 + first_claim;
+    c[1] = fixed ? G0 + first_claim : G0 + atomicAdd(work, 1);
 #pragma unroll
-    for (int j = 1; j < kClaimAhead; ++j) c[j] = G0 + atomicAdd(work, 1);
+    for (int j = 2; j < kClaimAhead; ++j) c[j] = G0 + atomicAdd(work, 1);
   }
   int k = 0;
   bool more = true;
@@ -483,11 +488,19 @@ __device__ void produce(const ApplyArgs& a, Smem& s, unsigned char* ring) {
 #pragma unroll
     for (int j = 0; j < kClaimAhead; ++j) {
       if (more) {
+        if (k == kStageAhead) {   // the first item goes out before the next claim is read
+          const int r = issue(0, true);
+          if (r <= 0) {
+            more = false;
+            P.ok = r == 0;
+            continue;
+          }
+        }
         const int v = __shfl_sync(kFull, c[j], 0);
         stage(v, k % kStage);
         if (lane == 0) c[j] = v < total ? G0 + atomicAdd(work, 1) : total;
-        if (k >= kStageAhead) {
-          const int r = issue((k - kStageAhead) % kStage);
+        if (k > kStageAhead) {
+          const int r = issue((k - kStageAhead) % kStage, false);
           if (r <= 0) {
             more = false;
             P.ok = r == 0;
@@ -586,44 +599,68 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
   // after it has completed.
   ptx::pdl_wait_prior_grid();
 
+  // The header check, the partition tables and the producer's first dynamic claim all
+  // go out at once: one round trip to L2 instead of one per dependent load.
   const Header* h = a.header;
+  int first_claim = 0;
+  if (t == kConsumers) first_claim = atomicAdd(const_cast<int*>(&h->work[0]), 1);
   if (t == 0) {   // one reader decides for the whole CTA
-    int go = h->status == EWG_OK;
-    if (go && (h->n != a.n || h->hidden != a.hidden || h->num_embeddings != a.num_embeddings)) {
+    const int status = h->status, hn = h->n, hh = h->hidden, np = h->num_parts, ep = h->epoch;
+    const long long hv = h->num_embeddings;
+    int go = status == EWG_OK;
+    if (go && (hn != a.n || hh != a.hidden || hv != a.num_embeddings)) {
       if (blockIdx.x == 0) const_cast<Header*>(h)->status = kStatusInvalid;
       go = 0;
     }
-    s.num_parts = go ? h->num_parts : -1;
-    s.epoch = h->epoch;
+    s.num_parts = go ? np : -1;
+    s.epoch = ep;
+  }
+  {   // counts (into prefix, scanned below) and offsets of the three lists
+    constexpr int kEntries = 3 * kMaxParts;
+    constexpr int kPer = (kEntries + kApplyThreads - 1) / kApplyThreads;
+    int cnt[kPer], off[kPer];
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = t + r * kApplyThreads;
+      const int list = i / kMaxParts, p = i - list * kMaxParts;
+      const int ct = list == 0 ? kLongCnt : list == 1 ? kShortCnt : kRunCnt;
+      const int ot = list == 0 ? kLongOff : list == 1 ? kShortOff : kRunOff;
+      cnt[r] = i < kEntries ? a.tables[ct * kMaxParts + p] : 0;
+      off[r] = i < kEntries ? a.tables[ot * kMaxParts + p] : 0;
+    }
+#pragma unroll
+    for (int r = 0; r < kPer; ++r) {
+      const int i = t + r * kApplyThreads;
+      if (i < kEntries) {
+        const int list = i / kMaxParts, p = i - list * kMaxParts;
+        s.prefix[list][p] = cnt[r];
+        s.offset[list][p] = off[r];
+      }
+    }
   }
   __syncthreads();
   if (s.num_parts < 0) return;
-  if (t < 32) {   // partition tables -> per-list prefix counts
-    const int parts = s.num_parts;
-    for (int list = 0; list < 3; ++list) {
-      const int cnt_tab = list == 0 ? kLongCnt : list == 1 ? kShortCnt : kRunCnt;
-      const int off_tab = list == 0 ? kLongOff : list == 1 ? kShortOff : kRunOff;
-      int carry = 0;
-      for (int p0 = 0; p0 < parts; p0 += 32) {
-        const int p = p0 + t;
-        const int c = p < parts ? a.tables[cnt_tab * kMaxParts + p] : 0;
-        if (p < parts) s.offset[list][p] = a.tables[off_tab * kMaxParts + p];
-        int x = c;
+  if (t < 3 * 32) {   // warp `list`: counts -> exclusive prefix, in place
+    const int list = t >> 5, lane = t & 31, parts = s.num_parts;
+    int carry = 0;
+    for (int p0 = 0; p0 < parts; p0 += 32) {
+      const int p = p0 + lane;
+      const int c = p < parts ? s.prefix[list][p] : 0;
+      int x = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(kFull, x, o);
-          if (t >= o) x += y;
-        }
-        if (p < parts) s.prefix[list][p] = carry + x - c;
-        carry += __shfl_sync(kFull, x, 31);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
       }
-      if (t == 0) s.prefix[list][parts] = carry;
+      if (p < parts) s.prefix[list][p] = carry + x - c;
+      carry += __shfl_sync(kFull, x, 31);
     }
+    if (lane == 0) s.prefix[list][parts] = carry;
   }
   __syncthreads();
 
   if (t >= kConsumers) {
-    produce<GBF16, MBF16>(a, s, ring);   // the whole producer warp
+    produce<GBF16, MBF16>(a, s, ring, first_claim);   // the whole producer warp
     return;
   }
   consume<GBF16, MBF16>(a, s, ring);
