@@ -1,5 +1,6 @@
 // C ABI of the library: argument checks, workspace layout and kernel launches.
 // The declarations and their contracts are in include/ewg.h.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -182,7 +183,7 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t row_be
 
 int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg, int mg_dtype,
              int64_t n, int64_t V, int64_t H, int64_t mg_row_stride, void* ws, int num_sms,
-             cudaStream_t stream) {
+             cudaStream_t stream, bool after_plan) {
   const ewg::Layout L = ewg::make_layout(n, H);
   ewg::ApplyArgs a{};
   a.grad = grad;
@@ -200,6 +201,11 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.runs = at<int>(ws, L.runs);
   a.partial = at<float>(ws, L.partial);
   a.arrivals = at<int>(ws, L.arrivals);
+  // Only when the plan of the same call runs just before (and every grad row is read):
+  // up to kPrefetchBytes of the first grad rows, at most half of them.
+  const int64_t grad_row_bytes = H * static_cast<int64_t>(elem_size(grad_dtype));
+  a.prefetch_rows =
+      after_plan ? static_cast<int>(std::min<int64_t>(n / 2, ewg::kPrefetchBytes / grad_row_bytes)) : 0;
   cudaError_t e = ewg::launch_apply(a, grad_dtype == EWG_BF16, mg_dtype == EWG_BF16, num_sms, stream);
   if (e != cudaSuccess) return cuda_fail(e, "apply launch");
   return EWG_OK;
@@ -250,7 +256,7 @@ int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const voi
   rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, 0, num_embeddings, hidden, workspace, s);
   if (rc) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
-                  num_embeddings, hidden, main_grad_row_stride, workspace, sms, s);
+                  num_embeddings, hidden, main_grad_row_stride, workspace, sms, s, true);
 }
 
 int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_embeddings,
@@ -283,7 +289,7 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* m
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
                   num_embeddings, hidden, main_grad_row_stride, workspace, sms,
-                  static_cast<cudaStream_t>(stream));
+                  static_cast<cudaStream_t>(stream), false);
 }
 
 int ewg_accumulate_shard(const void* ids, int ids_dtype, int64_t num_tokens, const void* grad,
@@ -306,7 +312,7 @@ int ewg_accumulate_shard(const void* ids, int ids_dtype, int64_t num_tokens, con
   rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, row_begin, shard_rows, hidden, workspace, s);
   if (rc) return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
-                  shard_rows, hidden, main_grad_row_stride, workspace, sms, s);
+                  shard_rows, hidden, main_grad_row_stride, workspace, sms, s, false);
 }
 
 int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_embeddings,

@@ -596,7 +596,18 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
     s.abort = 0;
   }
   // Launched early on the SMs the plan leaves free; the plan's lists are read only
-  // after it has completed.
+  // after it has completed.  Meanwhile the producer warp pulls this CTA's share of the
+  // first prefetch_rows grad rows into L2 (one bulk prefetch per row and lane).
+  if (t >= kConsumers && a.prefetch_rows > 0) {
+    const long long rows = a.prefetch_rows, G = gridDim.x;
+    const int r1 = static_cast<int>(rows * (blockIdx.x + 1) / G);
+    const uint32_t row_bytes = static_cast<uint32_t>(a.hidden) * (GBF16 ? 2u : 4u);
+    const uint64_t keep = ptx::policy_evict_last();
+    const char* g = static_cast<const char*>(a.grad);
+    for (int r = static_cast<int>(rows * blockIdx.x / G) + (t - kConsumers); r < r1; r += 32)
+      ptx::bulk_prefetch_l2(g + static_cast<long long>(r) * a.grad_stride * (GBF16 ? 2 : 4), row_bytes,
+                            keep);
+  }
   ptx::pdl_wait_prior_grid();
 
   // The header check, the partition tables and the producer's first dynamic claim all
