@@ -257,23 +257,25 @@ struct Producer {
     const uint32_t row_bytes = cols * (GBF16 ? 2 : 4);
     const uint32_t mg_bytes = is_long ? 0u : cols * (MBF16 ? 2 : 4);
     const uint32_t bytes = len * row_bytes + mg_bytes;
+    const char* src = nullptr;   // this lane's segment: grad row `lane`, or the main_grad row
+    if (lane < len) {
+      const long long p = d[kDescPos + lane];
+      src = static_cast<const char*>(a.grad) + (p * a.grad_stride + col0) * (GBF16 ? 2 : 4);
+    } else if (lane == len && !is_long) {
+      src = static_cast<const char*>(a.main_grad) +
+            (static_cast<long long>(id) * a.mg_stride + col0) * (MBF16 ? 2 : 4);
+    }
+    const uint32_t src_bytes = lane < len ? row_bytes : mg_bytes;
+    // The segments start towards L2 before the wait for ring space: the bytes a CTA has
+    // in flight are then not limited by its ring, and the copies below mostly hit L2.
+    if (src) ptx::bulk_prefetch_l2(src, src_bytes, pol);
     const int off = reserve(bytes);
     if (off < 0) return false;
     // for a long chunk, flags holds its index c in the run (prow - c: the run's counter)
     Item it{off, len, id, d[kDescPartial], col0, cols, is_long ? kLongChunk : kShortChunk,
             is_long ? (meta >> 4) : 0};
     uint64_t* bar = open(it, bytes);
-    if (lane < len) {
-      const long long p = d[kDescPos + lane];
-      const char* g = static_cast<const char*>(a.grad);
-      ptx::bulk_g2s(ring + off + lane * row_bytes, g + (p * a.grad_stride + col0) * (GBF16 ? 2 : 4),
-                    row_bytes, bar, pol);
-    } else if (lane == len && !is_long) {
-      const char* m = static_cast<const char*>(a.main_grad);
-      ptx::bulk_g2s(ring + off + len * row_bytes,
-                    m + (static_cast<long long>(id) * a.mg_stride + col0) * (MBF16 ? 2 : 4), mg_bytes,
-                    bar, pol);
-    }
+    if (src) ptx::bulk_g2s(ring + off + lane * row_bytes, src, src_bytes, bar, pol);
     return true;
   }
 
