@@ -60,11 +60,13 @@ struct Item {
   int off;        // byte offset of the item in the ring
   int rows;       // grad rows (chunks) or partial rows (combine) in the ring
   int id;         // main_grad row
-  int prow;       // partial row to write (long chunk), first partial row read (fold)
+  int prow;       // long chunk: its partial row (run's first + c); fold: the batch's block
+                  // of partial rows, in units of 128 floats
   int col0;       // first column
   int cols;       // columns
   int kind;
-  int flags;      // fold: bit 0 first batch, bit 1 last batch; long chunk: its index c
+  int flags;      // fold: bit 0 first batch, bit 1 last batch, slice width << 2;
+                  // long chunk: its index c in the run (and `id` holds the run's C)
 };
 
 struct Smem {
@@ -272,8 +274,8 @@ struct Producer {
     const int off = reserve(bytes);
     if (off < 0) return false;
     // for a long chunk, flags holds its index c in the run (prow - c: the run's counter)
-    Item it{off, len, id, d[kDescPartial], col0, cols, is_long ? kLongChunk : kShortChunk,
-            is_long ? (meta >> 4) : 0};
+    Item it{off, len, is_long ? d[kDescNumChunks] : id, d[kDescPartial], col0, cols,
+            is_long ? kLongChunk : kShortChunk, is_long ? (meta >> 4) : 0};
     uint64_t* bar = open(it, bytes);
     if (src) ptx::bulk_g2s(ring + off + lane * row_bytes, src, src_bytes, bar, pol);
     return true;
@@ -319,21 +321,25 @@ struct Producer {
       if (lane == 0) give_up(a, &s.abort);
       return false;
     }
-    const uint32_t row_bytes = cols * 4;
+    const uint32_t row_bytes = width * 4;   // the slice's partial rows are `width` apart
     const uint32_t mg_bytes = cols * (MBF16 ? 2 : 4);
     const int batch = min(kCombineBatch * split, 31);   // about 16 KB of partial rows
+    // the slice's block: C rows of `width` floats (a multiple of 128)
+    const long long block = static_cast<long long>(prow0) * partial_row_floats(a.hidden) +
+                            static_cast<long long>(C) * col0;
     for (int b0 = 0; b0 < C; b0 += batch) {
       const int nb = min(batch, C - b0);
       const bool last = b0 + nb == C;
       const uint32_t bytes = nb * row_bytes + (last ? mg_bytes : 0u);
       const int off = reserve(bytes);
       if (off < 0) return false;
-      Item it{off, nb, id, prow0 + b0, col0, cols, kCombine, (b0 == 0 ? 1 : 0) | (last ? 2 : 0)};
+      const long long at = block + static_cast<long long>(b0) * width;
+      Item it{off, nb, id, static_cast<int>(at / 128), col0, cols, kCombine,
+              (b0 == 0 ? 1 : 0) | (last ? 2 : 0) | (width << 2)};
       uint64_t* bar = open(it, bytes);
-      if (lane < nb) {
-        const float* src = a.partial + static_cast<long long>(prow0 + b0 + lane) * a.hidden + col0;
-        ptx::bulk_g2s(ring + off + lane * row_bytes, src, row_bytes, bar, pol);
-      } else if (lane == nb && last) {
+      if (lane == 0) {
+        ptx::bulk_g2s(ring + off, a.partial + at, nb * row_bytes, bar, pol);
+      } else if (lane == 1 && last) {
         const char* m = static_cast<const char*>(a.main_grad);
         ptx::bulk_g2s(ring + off + nb * row_bytes,
                       m + (static_cast<long long>(id) * a.mg_stride + col0) * (MBF16 ? 2 : 4),
@@ -534,8 +540,8 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
     const unsigned char* base = ring + it.off;
     if (it.kind == kCombine) {   // at most kCombineCols <= 8 * kConsumers columns
       const int c = t * 8;
+      const uint32_t row_bytes = (it.flags >> 2) * 4;   // slice width apart
       if (c < it.cols) {
-        const uint32_t row_bytes = it.cols * 4;
         if (it.flags & 1) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) total[e] = 0.0f;   // "in order starting from 0"
@@ -544,12 +550,13 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
         if (it.flags & 2)
           finish<GBF16, MBF16>(a, total, base + it.rows * row_bytes + c * (MBF16 ? 2 : 4), it.id,
                                it.col0 + c);
-        // The batch's partial rows are dead now: drop their L2 lines instead of writing
-        // them back.  Only when every fold slice is whole 128-byte lines (hidden % 32 == 0:
-        // rows and the 128-column slices then start on line boundaries).
-        if ((a.hidden & 31) == 0 && (c & 31) == 0)
-          for (int k = 0; k < it.rows; ++k)
-            ptx::discard_l2_line(a.partial + static_cast<long long>(it.prow + k) * a.hidden + it.col0 + c);
+      }
+      // The batch's partial rows are dead now: drop their L2 lines (the block is whole
+      // 128-byte lines) instead of writing them back.
+      {
+        const float* blk = a.partial + static_cast<long long>(it.prow) * 128;
+        const int lines = it.rows * static_cast<int>(row_bytes) / 128;
+        for (int l = t; l < lines; l += kConsumers) ptx::discard_l2_line(blk + l * 32);
       }
     } else {   // chunk item: passes of 8 * kConsumers columns over the tile
       const uint32_t row_bytes = it.cols * (GBF16 ? 2 : 4);
@@ -560,8 +567,12 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
         for (int k = 0; k < it.rows; ++k)
           add_row<GBF16>(part, base + k * row_bytes + c * (GBF16 ? 2 : 4));
         if (it.kind == kLongChunk) {
-          // partial rows are read back soon by the run's fold: ask L2 to keep them
-          float* dst = a.partial + static_cast<long long>(it.prow) * a.hidden + it.col0 + c;
+          // partial rows are read back soon by the run's fold: ask L2 to keep them.  Slice-
+          // major: chunk c's slice [s, s + w) at C s + c w in the run's floats.
+          const int C = it.id, ci = it.flags, w = kCombineCols / fold_entries(C);
+          const int col = it.col0 + c, s0 = col & ~(w - 1);
+          float* dst = a.partial + static_cast<long long>(it.prow - ci) * partial_row_floats(a.hidden) +
+                       static_cast<long long>(C) * s0 + static_cast<long long>(ci) * w + (col - s0);
           ptx::st_global_v4(dst, part[0], part[1], part[2], part[3], pol_keep);
           ptx::st_global_v4(dst + 4, part[4], part[5], part[6], part[7], pol_keep);
         } else {   // the run's only chunk: t = 0 + part

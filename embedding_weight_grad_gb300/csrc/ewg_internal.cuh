@@ -114,6 +114,15 @@ static_assert(sizeof(Header) == 256, "header is one 256-byte region");
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// fp32 partial rows, kept slice-major per run: the run whose first partial row is p0
+// owns floats [p0 P, (p0 + C) P) of the region, P = partial_row_floats(hidden); in
+// them, column slice [s, s + w) (w = kCombineCols / fold_entries(C), s a multiple of w)
+// of chunk c sits at C s + c w.  A fold batch (consecutive chunks, one slice) is then
+// one contiguous block.
+__host__ __device__ inline int64_t partial_row_floats(int64_t hidden) {
+  return (hidden + kCombineCols - 1) / kCombineCols * kCombineCols;
+}
+
 // Long runs of L >= 11 rows have ceil(L/10) <= 2L/11 chunks; partition b of the hashed
 // plan starts its partial rows at floor(2 S_b / 11) + b (S_b: tokens of partitions < b).
 inline int64_t max_partial_rows(int64_t n) { return 2 * n / 11 + kMaxParts + 1; }
@@ -152,7 +161,7 @@ inline Layout make_layout(int64_t n, int64_t hidden) {
   L.tile_bad = take(static_cast<size_t>(L.tiles) * 4);
   L.tile_cnt = take(static_cast<size_t>(L.tiles) * 16);
   L.arrivals = take(static_cast<size_t>(max_partial_rows(n)) * 4);
-  L.partial = take(static_cast<size_t>(max_partial_rows(n)) * hidden * 4);
+  L.partial = take(static_cast<size_t>(max_partial_rows(n)) * partial_row_floats(hidden) * 4);
   L.total = off;
   return L;
 }
