@@ -2,11 +2,12 @@
 //
 // Some callers cannot allocate device memory at the moment they need the gradient
 // accumulated: code running under a custom or fixed-pool allocator that must not grow,
-// inference-style runtimes that forbid cudaMalloc after start-up, or hooks called from
-// inside a CUDA graph region.  For them this file owns a fixed block of device memory,
-// a file-scope __device__ array, and uses it as the workspace of ewg_accumulate.  The
-// block is reserved on every device that loads the library and kept until the process
-// exits.  Calls are limited to sizes whose workspace fits in it.
+// and runtimes that forbid cudaMalloc after start-up.  For them this file owns a fixed
+// block of device memory, a file-scope __device__ array, and uses it as the workspace of
+// ewg_accumulate.  The block is reserved on every device that loads the library and kept
+// until the process exits.  Calls are limited to sizes whose workspace fits in it.  The
+// first call on a device looks up the block's device address (make it outside any
+// stream capture); calls that overlap on the GPU race on the block.
 #include <mutex>
 
 #include "ewg.h"

@@ -190,9 +190,8 @@ int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens,
  * has no counterpart; this is an addition for callers that cannot allocate.)
  *
  * For callers that cannot allocate device memory when the gradient is accumulated:
- * code running under a fixed-pool or custom allocator that must not grow, runtimes
- * that forbid cudaMalloc after start-up, hooks called while a CUDA graph is being
- * recorded.  The library keeps a file-scope __device__ array of
+ * code running under a fixed-pool or custom allocator that must not grow, and runtimes
+ * that forbid cudaMalloc after start-up.  The library keeps a file-scope __device__ array of
  * EWG_STATIC_SCRATCH_BYTES as the workspace; every device that loads the library
  * holds it until the process exits.  Arguments and results are those of
  * ewg_accumulate, without the workspace.
