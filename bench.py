@@ -183,13 +183,17 @@ def traffic_from_profile(kernel_src_hash: str):
     return d.get("dram_bytes_per_launch")
 
 
+# the files the apply kernel is compiled from
+APPLY_SOURCES = ("embedding_weight_grad_gb300/csrc/ewg_apply.cu",
+                 "embedding_weight_grad_gb300/csrc/ewg_internal.cuh",
+                 "embedding_weight_grad_gb300/csrc/ewg_ptx.cuh")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "embedding_weight_grad_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(fh.read())
+    for f in APPLY_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()
 
 
