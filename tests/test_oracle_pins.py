@@ -238,3 +238,20 @@ def test_workload_recipe_shapes():
     ids = workloads.make_ids(lr).reshape(-1)
     assert (ids == lr.num_embeddings - 1).sum() >= round(0.2 * ids.size)
     assert np.array_equal(workloads.make_ids(lr).reshape(-1), ids)   # seeded
+
+
+def test_zipf_recipe_frequencies():
+    """The Zipf ids follow P(id = k - 1) proportional to k**-s: the counts of the first
+    ranks lie within 5 standard deviations of n P, computed here from the closed-form
+    normaliser (a partial zeta sum), and hot ids are the small ones."""
+    rng = np.random.default_rng(7)
+    V, s, n = 129280, 1.1, 200000
+    ids = workloads.zipf_ids(rng, V, s, n)
+    norm = float(np.sum(np.arange(1, V + 1, dtype=np.float64) ** -s))
+    counts = np.bincount(ids, minlength=V)
+    for k in range(1, 6):
+        p = k ** -s / norm
+        mean, sd = n * p, (n * p * (1 - p)) ** 0.5
+        assert abs(counts[k - 1] - mean) < 5 * sd, (k, counts[k - 1], mean)
+    assert counts[0] > counts[1] > counts[2] > counts[10]
+    assert ids.min() >= 0 and ids.max() < V
