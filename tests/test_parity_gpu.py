@@ -134,6 +134,7 @@ def make(n, V, H, gdt=torch.bfloat16, mdt=torch.float32, seed=0, ids=None):
     (5000, 1, 64),             # one token id: a single 5000-row run, no radix pass
     (4100, 2, 128),            # two ids: two long runs
     (12000, 40000, 72),        # mostly single-occurrence runs
+    (140000, 100000, 8),       # more than 64 tiles: the one-CTA scan kernels of the sort
 ])
 def test_shapes_and_id_patterns(oracle_mod, n, V, H):
     run_case(oracle_mod, *make(n, V, H, seed=n))
