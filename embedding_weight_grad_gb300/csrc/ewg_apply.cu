@@ -16,11 +16,12 @@
 // rows are normally complete when it is claimed; a fold still waits (bounded) on its
 // run's arrival counter, which each consumer warp bumps after storing its partial
 // columns.  Within a CTA a producer warp issues cp.async.bulk copies of the gathered
-// grad row segments (or partial rows) and of the main_grad segment into a shared-memory
-// ring, one lane per row, completing on a per-slot mbarrier; four consumer warps (8
-// columns per thread) take the slots in order, add the rows in order from shared memory
-// and release the slot.  The depth of the ring, not the register file, sets how many bytes
-// each SM keeps in flight.
+// grad row segments (one lane per row) and of the main_grad segment, or of a fold batch
+// (one contiguous block of partial rows), into a shared-memory ring, completing on a
+// per-slot mbarrier; four consumer warps (8 columns per thread) take the slots in order,
+// add the rows in order from shared memory and release the slot.  Each item's segments
+// are also requested into L2 before the producer waits for ring space, so the bytes an SM
+// keeps in flight are not bounded by its rings.
 #include <cuda_bf16.h>
 
 #include "ewg.h"
@@ -61,7 +62,7 @@ struct Item {
   int rows;       // grad rows (chunks) or partial rows (combine) in the ring
   int id;         // main_grad row
   int prow;       // long chunk: its partial row (run's first + c); fold: the batch's block
-                  // of partial rows, in units of 128 floats
+                  // of partial rows, in 128-byte lines
   int col0;       // first column
   int cols;       // columns
   int kind;
@@ -309,8 +310,9 @@ struct Producer {
   }
 
   // One fold: a column slice (the whole 512-column group, or the entry's 1/split of it)
-  // of a long run, as batches of partial rows (lane k: row k of the batch); the last
-  // batch also brings the main_grad segment.
+  // of a long run, as batches of consecutive partial rows, each one bulk copy of a
+  // contiguous block (partial rows are slice-major); the last batch also brings the
+  // main_grad segment.
   __device__ bool combine_task(const int* run, int group, int Tl) {
     const int prow0 = run[0], C = run[1], id = run[2];
     const int split = run[3] >> 4, width = kCombineCols / split;
@@ -324,7 +326,7 @@ struct Producer {
     const uint32_t row_bytes = width * 4;   // the slice's partial rows are `width` apart
     const uint32_t mg_bytes = cols * (MBF16 ? 2 : 4);
     const int batch = min(kCombineBatch * split, 31);   // about 16 KB of partial rows
-    // the slice's block: C rows of `width` floats (a multiple of 128)
+    // the slice's block: C rows of `width` floats (a multiple of 32: whole 128-byte lines)
     const long long block = static_cast<long long>(prow0) * partial_row_floats(a.hidden) +
                             static_cast<long long>(C) * col0;
     for (int b0 = 0; b0 < C; b0 += batch) {
@@ -334,7 +336,7 @@ struct Producer {
       const int off = reserve(bytes);
       if (off < 0) return false;
       const long long at = block + static_cast<long long>(b0) * width;
-      Item it{off, nb, id, static_cast<int>(at / 128), col0, cols, kCombine,
+      Item it{off, nb, id, static_cast<int>(at / 32), col0, cols, kCombine,
               (b0 == 0 ? 1 : 0) | (last ? 2 : 0) | (width << 2)};
       uint64_t* bar = open(it, bytes);
       if (lane == 0) {
@@ -554,7 +556,7 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
       // The batch's partial rows are dead now: drop their L2 lines (the block is whole
       // 128-byte lines) instead of writing them back.
       {
-        const float* blk = a.partial + static_cast<long long>(it.prow) * 128;
+        const float* blk = a.partial + static_cast<long long>(it.prow) * 32;
         const int lines = it.rows * static_cast<int>(row_bytes) / 128;
         for (int l = t; l < lines; l += kConsumers) ptx::discard_l2_line(blk + l * 32);
       }
