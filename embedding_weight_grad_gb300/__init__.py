@@ -77,6 +77,11 @@ def lib():
             L.ewg_accumulate_shard.restype = i32
             L.ewg_plan_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, sz, vp]
             L.ewg_plan_shard.restype = i32
+            L.ewg_host_workspace_bytes.argtypes = [i64, i64, i32, i32]
+            L.ewg_host_workspace_bytes.restype = sz
+            L.ewg_accumulate_host.argtypes = [vp, i32, i64, vp, i32, vp, i32, i64, i64, i64, vp,
+                                              sz, vp]
+            L.ewg_accumulate_host.restype = i32
             L.ewg_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
             L.ewg_read_status.restype = i32
             L.ewg_status_string.argtypes = [i32]
@@ -192,6 +197,50 @@ def accumulate_embedding_wgrad(ids: torch.Tensor, grad: torch.Tensor, main_grad:
         ws = workspace if workspace is not None else new_workspace(a.n, a.H, a.device)
         stream = _stream_ptr(a.device)
         _raise_on(L.ewg_accumulate(*a.c_args(), ws.data_ptr(), ws.numel(), stream))
+        if check:
+            raise_on_device_status(ws)
+
+
+def new_host_workspace(num_tokens: int, hidden: int, ids_dtype: torch.dtype,
+                       grad_dtype: torch.dtype, device=None) -> torch.Tensor:
+    """A device buffer for accumulate_embedding_wgrad_from_host with these sizes and dtypes."""
+    nbytes = int(lib().ewg_host_workspace_bytes(num_tokens, hidden, _ID_CODES.get(ids_dtype, -1),
+                                                _FLOAT_CODES.get(grad_dtype, -1)))
+    if nbytes == 0:
+        raise EwgError(ERR_UNSUPPORTED, "unsupported num_tokens / hidden / dtypes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def accumulate_embedding_wgrad_from_host(ids: torch.Tensor, grad: torch.Tensor,
+                                         main_grad: torch.Tensor, *,
+                                         workspace: torch.Tensor | None = None,
+                                         check: bool = False) -> None:
+    """accumulate_embedding_wgrad with ids and grad in pinned host memory: the library
+    copies them to the device (the grad copy overlapping the plan) and accumulates into
+    main_grad on its device, all enqueued on the current stream.  ids: contiguous CPU
+    int32/int64 tensor, grad: contiguous CPU bf16/fp32 tensor [*ids.shape, hidden], both
+    pinned; main_grad: CUDA [num_embeddings, hidden].  check=True as in
+    accumulate_embedding_wgrad."""
+    if ids.is_cuda or grad.is_cuda or not main_grad.is_cuda:
+        raise ValueError("ids and grad must be host tensors, main_grad a CUDA tensor")
+    if not (ids.is_contiguous() and grad.is_contiguous() and ids.is_pinned() and grad.is_pinned()):
+        raise ValueError("ids and grad must be contiguous pinned host tensors")
+    if ids.dtype not in _ID_CODES or grad.dtype not in _FLOAT_CODES \
+            or main_grad.dtype not in _FLOAT_CODES or main_grad.dim() != 2 or main_grad.stride(1) != 1:
+        raise ValueError("unsupported dtypes or main_grad layout")
+    V, H = main_grad.shape
+    n = ids.numel()
+    if tuple(grad.shape) != tuple(ids.shape) + (H,):
+        raise ValueError("grad must be [*ids.shape, hidden]")
+    with torch.cuda.device(main_grad.device):
+        L = lib()
+        ws = workspace if workspace is not None else new_host_workspace(n, H, ids.dtype, grad.dtype,
+                                                                        main_grad.device)
+        _raise_on(L.ewg_accumulate_host(
+            ids.data_ptr(), _ID_CODES[ids.dtype], n, grad.data_ptr(), _FLOAT_CODES[grad.dtype],
+            main_grad.data_ptr(), _FLOAT_CODES[main_grad.dtype], V, H,
+            main_grad.stride(0) if V > 1 else H, ws.data_ptr(), ws.numel(),
+            _stream_ptr(main_grad.device)))
         if check:
             raise_on_device_status(ws)
 

@@ -27,6 +27,9 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
+  // ewg_accumulate_host: the stream the grad copy runs on, and the events that order it
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t queued = nullptr, grad_in = nullptr;
 };
 
 std::mutex g_mu;
@@ -217,6 +220,29 @@ int check_shard(int64_t V, int64_t row_begin, int64_t rows) {
   return EWG_OK;
 }
 
+// Layout of the host-input workspace: the ordinary workspace, then the copies of ids and
+// grad, each 256-byte aligned.
+struct HostLayout {
+  size_t ids, grad, total;
+};
+
+HostLayout host_layout(int64_t n, int64_t H, int ids_dtype, int grad_dtype) {
+  HostLayout L{};
+  L.ids = ewg::make_layout(n, H).total;
+  L.grad = ewg::align_up(L.ids + static_cast<size_t>(n) * elem_size(ids_dtype), 256);
+  L.total = ewg::align_up(L.grad + static_cast<size_t>(n) * H * elem_size(grad_dtype), 256);
+  return L;
+}
+
+bool pinned_host(const void* p) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeHost;
+}
+
 }  // namespace
 
 void ewg::set_last_error(const char* msg) { g_last_error = msg; }
@@ -354,6 +380,70 @@ const char* ewg_status_string(int status) {
     case EWG_ERR_TIMEOUT: return "EWG_ERR_TIMEOUT";
     default: return "EWG_ERR_UNKNOWN";
   }
+}
+
+size_t ewg_host_workspace_bytes(int64_t num_tokens, int64_t hidden, int ids_dtype,
+                                int grad_dtype) {
+  if (ewg_workspace_bytes(num_tokens, hidden) == 0) return 0;
+  if ((ids_dtype != EWG_INT32 && ids_dtype != EWG_INT64) ||
+      (grad_dtype != EWG_BF16 && grad_dtype != EWG_FP32))
+    return 0;
+  return host_layout(num_tokens, hidden, ids_dtype, grad_dtype).total;
+}
+
+int ewg_accumulate_host(const void* ids_host, int ids_dtype, int64_t num_tokens,
+                        const void* grad_host, int grad_dtype, void* main_grad,
+                        int main_grad_dtype, int64_t num_embeddings, int64_t hidden,
+                        int64_t main_grad_row_stride, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+  g_last_error.clear();
+  int dev = 0, sms = 0;
+  int rc = current_device(&dev, &sms);
+  if (rc) return rc;
+  if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
+  if (ids_dtype != EWG_INT32 && ids_dtype != EWG_INT64)
+    return fail(EWG_ERR_UNSUPPORTED, "ids must be int32 or int64");
+  if (grad_dtype != EWG_BF16 && grad_dtype != EWG_FP32)
+    return fail(EWG_ERR_UNSUPPORTED, "grad must be bf16 or fp32");
+  if (!ids_host || !grad_host || !pinned_host(ids_host) || !pinned_host(grad_host))
+    return fail(EWG_ERR_UNSUPPORTED, "ids_host and grad_host must be page-locked host memory");
+  if ((rc = check_mat(main_grad, main_grad_dtype, main_grad_row_stride, hidden, dev, "main_grad")))
+    return rc;
+  const HostLayout HL = host_layout(num_tokens, hidden, ids_dtype, grad_dtype);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < HL.total || !on_device(workspace, dev))
+    return fail(EWG_ERR_INVALID, "workspace null, misaligned, not on the device or smaller than ewg_host_workspace_bytes");
+  if (overlap(span(main_grad, num_embeddings, hidden, main_grad_row_stride, elem_size(main_grad_dtype)),
+              {reinterpret_cast<uintptr_t>(workspace), reinterpret_cast<uintptr_t>(workspace) + HL.total}))
+    return fail(EWG_ERR_UNSUPPORTED, "main_grad overlaps the workspace");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  const size_t ids_bytes = static_cast<size_t>(num_tokens) * elem_size(ids_dtype);
+  const size_t grad_bytes = static_cast<size_t>(num_tokens) * hidden * elem_size(grad_dtype);
+
+  std::lock_guard<std::mutex> lock(g_mu);   // the copy stream and events are shared
+  DeviceState& d = g_devices[dev];
+  cudaError_t e = cudaSuccess;
+  if (!d.copy_stream) {
+    e = cudaStreamCreateWithFlags(&d.copy_stream, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.queued, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d.grad_in, cudaEventDisableTiming);
+    if (e != cudaSuccess) return cuda_fail(e, "copy stream set-up");
+  }
+  // The grad copy starts after the work already queued on `stream` (an earlier call may
+  // still read this workspace) and overlaps the ids copy and the plan.
+  e = cudaEventRecord(d.queued, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(d.copy_stream, d.queued, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ws + HL.grad, grad_host, grad_bytes, cudaMemcpyHostToDevice, d.copy_stream);
+  if (e == cudaSuccess) e = cudaEventRecord(d.grad_in, d.copy_stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ws + HL.ids, ids_host, ids_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "host input copies");
+  rc = do_plan(ws + HL.ids, ids_dtype, num_tokens, num_embeddings, 0, num_embeddings, hidden, workspace, s);
+  if (rc) return rc;
+  e = cudaStreamWaitEvent(s, d.grad_in, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamWaitEvent");
+  return do_apply(ws + HL.grad, grad_dtype, hidden, main_grad, main_grad_dtype, num_tokens,
+                  num_embeddings, hidden, main_grad_row_stride, workspace, sms, s, false);
 }
 
 const char* ewg_last_error(void) { return g_last_error.c_str(); }

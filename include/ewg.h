@@ -182,6 +182,31 @@ int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens,
                    int64_t num_embeddings, int64_t row_begin, int64_t shard_rows,
                    int64_t hidden, void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * ewg_accumulate with ids and grad in pinned host memory (the page's function takes
+ * device tensors; this is the same call for a caller whose inputs start on the host).
+ *
+ * ids_host: num_tokens ids (EWG_INT32 or EWG_INT64), contiguous; grad_host:
+ * [num_tokens, hidden] (EWG_BF16 or EWG_FP32), contiguous (row stride = hidden).  Both
+ * must be page-locked host memory (cudaHostAlloc / cudaHostRegister / a pinned torch
+ * tensor), else EWG_ERR_UNSUPPORTED.  main_grad: a device matrix as in ewg_accumulate.
+ * workspace: device memory of at least ewg_host_workspace_bytes(...) bytes; it receives
+ * the copies of ids and grad next to the ordinary workspace.
+ *
+ * Stream-ordered on `stream`: the ids are copied and planned on `stream` while the grad
+ * copy runs on a library-owned stream of the device (made on the first call, after the
+ * work already queued on `stream`); the apply waits for both.  Calls on one device from
+ * several host threads are serialised by the library while they enqueue.  Errors and
+ * the device status: as ewg_accumulate (ewg_read_status on the same workspace).
+ */
+size_t ewg_host_workspace_bytes(int64_t num_tokens, int64_t hidden, int ids_dtype,
+                                int grad_dtype);
+int ewg_accumulate_host(const void* ids_host, int ids_dtype, int64_t num_tokens,
+                        const void* grad_host, int grad_dtype, void* main_grad,
+                        int main_grad_dtype, int64_t num_embeddings, int64_t hidden,
+                        int64_t main_grad_row_stride, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
 /* Size of the library-owned scratch used by ewg_accumulate_static (64 MiB). */
 #define EWG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
