@@ -79,6 +79,19 @@ def test_workspace_bytes(lib):
     assert ewg.workspace_bytes(8192, 7168) < ewg.workspace_bytes(8192, 7176)
 
 
+def test_host_workspace_bytes(lib):
+    # the ordinary workspace plus 256-aligned copies of ids and grad; 0 when unsupported
+    n, h = 8192, 7168
+    base = ewg.workspace_bytes(n, h)
+    got = lib.ewg_host_workspace_bytes(n, h, 1, 2)          # int64 ids, bf16 grad
+    assert got % 256 == 0 and got >= base + n * 8 + n * h * 2
+    assert got < base + n * 8 + n * h * 2 + 512
+    assert lib.ewg_host_workspace_bytes(n, h, 0, 3) >= base + n * 4 + n * h * 4
+    assert lib.ewg_host_workspace_bytes(n, h, 2, 2) == 0     # ids dtype not an integer
+    assert lib.ewg_host_workspace_bytes(n, h, 1, 1) == 0     # grad dtype not a float
+    assert lib.ewg_host_workspace_bytes(0, h, 1, 2) == 0
+
+
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     """With the shared library absent the binding raises instead of computing anything."""
     import importlib
