@@ -30,12 +30,17 @@ MAX_TOKENS = 1 << 28
 NROWS = 10
 
 _INT32, _INT64, _BF16, _FP32 = 0, 1, 2, 3
-OK, ERR_UNSUPPORTED, ERR_INVALID, ERR_CUDA, ERR_ID_OUT_OF_RANGE = 0, 1, 2, 3, 4
+OK, ERR_UNSUPPORTED, ERR_INVALID, ERR_CUDA, ERR_ID_OUT_OF_RANGE, ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libewg.so")
 _lib = None
 _lock = threading.Lock()
+# Pinned host tensors handed to the host-input call, each kept alive until an event
+# recorded after the call has completed: the library copies from their raw pointers, so
+# torch's pinned-memory allocator does not know the copies are still pending.
+_pending_host = []
+_pending_lock = threading.Lock()
 
 
 class EwgError(RuntimeError):
@@ -211,6 +216,16 @@ def new_host_workspace(num_tokens: int, hidden: int, ids_dtype: torch.dtype,
     return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
 
 
+def _keep_until_passed(stream, tensors) -> None:
+    """Holds `tensors` until `stream` has passed the work enqueued so far; entries whose
+    event has completed are dropped on every call."""
+    ev = torch.cuda.Event()
+    ev.record(stream)
+    with _pending_lock:
+        _pending_host[:] = [(e, t) for (e, t) in _pending_host if not e.query()]
+        _pending_host.append((ev, tensors))
+
+
 def accumulate_embedding_wgrad_from_host(ids: torch.Tensor, grad: torch.Tensor,
                                          main_grad: torch.Tensor, *,
                                          workspace: torch.Tensor | None = None,
@@ -220,7 +235,12 @@ def accumulate_embedding_wgrad_from_host(ids: torch.Tensor, grad: torch.Tensor,
     main_grad on its device, all enqueued on the current stream.  ids: contiguous CPU
     int32/int64 tensor, grad: contiguous CPU bf16/fp32 tensor [*ids.shape, hidden], both
     pinned; main_grad: CUDA [num_embeddings, hidden].  check=True as in
-    accumulate_embedding_wgrad."""
+    accumulate_embedding_wgrad.
+
+    The copies run after the call returns.  This function keeps ids and grad alive until
+    the stream has passed the call, so dropping them (or a temporary ``x.pin_memory()``)
+    right away is safe; writing new values into them before the stream has passed the
+    call is not (synchronize the stream, or wait on an event recorded after the call)."""
     if ids.is_cuda or grad.is_cuda or not main_grad.is_cuda:
         raise ValueError("ids and grad must be host tensors, main_grad a CUDA tensor")
     if not (ids.is_contiguous() and grad.is_contiguous() and ids.is_pinned() and grad.is_pinned()):
@@ -241,6 +261,7 @@ def accumulate_embedding_wgrad_from_host(ids: torch.Tensor, grad: torch.Tensor,
             main_grad.data_ptr(), _FLOAT_CODES[main_grad.dtype], V, H,
             main_grad.stride(0) if V > 1 else H, ws.data_ptr(), ws.numel(),
             _stream_ptr(main_grad.device)))
+        _keep_until_passed(torch.cuda.current_stream(main_grad.device), (ids, grad))
         if check:
             raise_on_device_status(ws)
 

@@ -6,6 +6,8 @@
 #include <mutex>
 #include <string>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "ewg.h"
 #include "ewg_internal.cuh"
 
@@ -141,6 +143,23 @@ int check_workspace(void* ws, size_t bytes, int64_t n, int64_t H, int dev) {
   return EWG_OK;
 }
 
+// The plan and apply kernels write the workspace while they read ids and grad and
+// update main_grad, so none of these may share bytes with it.
+int check_apart(const void* ws, int64_t n, int64_t H, Range r, const char* what) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(ws);
+  if (overlap(r, {lo, lo + ewg::make_layout(n, H).total}))
+    return fail(EWG_ERR_UNSUPPORTED, std::string(what) + " overlaps the workspace");
+  return EWG_OK;
+}
+
+Range ids_span(const void* ids, int ids_dtype, int64_t n) { return span(ids, 1, n, n, elem_size(ids_dtype)); }
+
+// Marks the host-side enqueue of one step in profiler timelines (a no-op without a tool).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
@@ -150,6 +169,7 @@ T* at(void* ws, size_t off) {
 // row_begin = 0, rows = V).
 int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t row_begin,
             int64_t rows, int64_t H, void* ws, cudaStream_t stream) {
+  NvtxRange range("ewg_plan");
   const ewg::Layout L = ewg::make_layout(n, H);
   const bool sharded = row_begin != 0 || rows != V;
   // a skipped id sorts as key `rows`, after the shard's own keys
@@ -187,6 +207,7 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t row_be
 int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg, int mg_dtype,
              int64_t n, int64_t V, int64_t H, int64_t mg_row_stride, void* ws, int num_sms,
              cudaStream_t stream, bool after_plan) {
+  NvtxRange range("ewg_apply");
   const ewg::Layout L = ewg::make_layout(n, H);
   ewg::ApplyArgs a{};
   a.grad = grad;
@@ -278,6 +299,13 @@ int ewg_accumulate(const void* ids, int ids_dtype, int64_t num_tokens, const voi
                  main_grad_dtype, num_embeddings, hidden, main_grad_row_stride, dev);
   if (rc) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  if ((rc = check_apart(workspace, num_tokens, hidden, ids_span(ids, ids_dtype, num_tokens), "ids")) ||
+      (rc = check_apart(workspace, num_tokens, hidden,
+                        span(grad, num_tokens, hidden, grad_row_stride, elem_size(grad_dtype)), "grad")) ||
+      (rc = check_apart(workspace, num_tokens, hidden,
+                        span(main_grad, num_embeddings, hidden, main_grad_row_stride, elem_size(main_grad_dtype)),
+                        "main_grad")))
+    return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, 0, num_embeddings, hidden, workspace, s);
   if (rc) return rc;
@@ -294,6 +322,8 @@ int ewg_plan(const void* ids, int ids_dtype, int64_t num_tokens, int64_t num_emb
   if ((rc = check_sizes(num_tokens, num_embeddings, hidden))) return rc;
   if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  if ((rc = check_apart(workspace, num_tokens, hidden, ids_span(ids, ids_dtype, num_tokens), "ids")))
+    return rc;
   return do_plan(ids, ids_dtype, num_tokens, num_embeddings, 0, num_embeddings, hidden, workspace,
                  static_cast<cudaStream_t>(stream));
 }
@@ -313,6 +343,12 @@ int ewg_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* m
               span(grad, num_tokens, hidden, grad_row_stride, elem_size(grad_dtype))))
     return fail(EWG_ERR_UNSUPPORTED, "main_grad overlaps grad");
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  if ((rc = check_apart(workspace, num_tokens, hidden,
+                        span(grad, num_tokens, hidden, grad_row_stride, elem_size(grad_dtype)), "grad")) ||
+      (rc = check_apart(workspace, num_tokens, hidden,
+                        span(main_grad, num_embeddings, hidden, main_grad_row_stride, elem_size(main_grad_dtype)),
+                        "main_grad")))
+    return rc;
   return do_apply(grad, grad_dtype, grad_row_stride, main_grad, main_grad_dtype, num_tokens,
                   num_embeddings, hidden, main_grad_row_stride, workspace, sms,
                   static_cast<cudaStream_t>(stream), false);
@@ -334,6 +370,13 @@ int ewg_accumulate_shard(const void* ids, int ids_dtype, int64_t num_tokens, con
                  main_grad_dtype, shard_rows, hidden, main_grad_row_stride, dev);
   if (rc) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  if ((rc = check_apart(workspace, num_tokens, hidden, ids_span(ids, ids_dtype, num_tokens), "ids")) ||
+      (rc = check_apart(workspace, num_tokens, hidden,
+                        span(grad, num_tokens, hidden, grad_row_stride, elem_size(grad_dtype)), "grad")) ||
+      (rc = check_apart(workspace, num_tokens, hidden,
+                        span(main_grad, shard_rows, hidden, main_grad_row_stride, elem_size(main_grad_dtype)),
+                        "main_grad")))
+    return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   rc = do_plan(ids, ids_dtype, num_tokens, num_embeddings, row_begin, shard_rows, hidden, workspace, s);
   if (rc) return rc;
@@ -352,6 +395,8 @@ int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens, int64_t n
   if ((rc = check_shard(num_embeddings, row_begin, shard_rows))) return rc;
   if ((rc = check_ids(ids, ids_dtype, dev))) return rc;
   if ((rc = check_workspace(workspace, workspace_bytes, num_tokens, hidden, dev))) return rc;
+  if ((rc = check_apart(workspace, num_tokens, hidden, ids_span(ids, ids_dtype, num_tokens), "ids")))
+    return rc;
   return do_plan(ids, ids_dtype, num_tokens, num_embeddings, row_begin, shard_rows, hidden,
                  workspace, static_cast<cudaStream_t>(stream));
 }

@@ -82,6 +82,7 @@ struct Smem {
   int num_parts;
   int abort;
   int epoch;      // apply calls already made on this plan
+  int spin_limit; // polls of a fold's arrival counter before it gives up
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -283,21 +284,23 @@ struct Producer {
   }
 
   // Waits until every consumer warp that handled a chunk item of the run has stored its
-  // partial columns: C chunks x Tl column tiles x kConsumerWarps arrivals.  Lane 0 spins
-  // (bounded); then every lane acquires the counter itself, so its later bulk copies of
-  // the partial rows (async proxy) come after the rows' generic-proxy stores.
+  // partial columns: C chunks x Tl column tiles x kConsumerWarps arrivals.  Lane 0 polls
+  // (at most spin_limit times, and it stops early once this CTA or any other has given
+  // up); then every lane acquires the counter itself, so its later bulk copies of the
+  // partial rows (async proxy) come after the rows' generic-proxy stores.
   __device__ bool wait_run(int prow0, int target) {
     const int* cnt = a.arrivals + prow0;
+    const volatile int* status = &a.header->status;
     int got = 0;
     if (lane == 0) {
-      for (uint32_t i = 0; i < kSpinLimit; ++i) {
+      for (int i = 0; i < s.spin_limit; ++i) {
         int v;
         asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
         if (v >= target) {
           got = 1;
           break;
         }
-        if ((i & 255u) == 255u && s.abort) break;
+        if ((i & 63) == 63 && (s.abort || *status == kStatusTimeout)) break;
         __nanosleep(64);
       }
     }
@@ -631,7 +634,8 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
   int first_claim = 0;
   if (t == kConsumers) first_claim = atomicAdd(const_cast<int*>(&h->work[0]), 1);
   if (t == 0) {   // one reader decides for the whole CTA
-    const int status = h->status, hn = h->n, hh = h->hidden, np = h->num_parts, ep = h->epoch;
+    const int status = h->status, hn = h->n, hh = h->hidden, np = h->num_parts, ep = h->epoch,
+              sl = h->spin_limit;
     const long long hv = h->num_embeddings;
     int go = status == EWG_OK;
     if (go && (hn != a.n || hh != a.hidden || hv != a.num_embeddings)) {
@@ -640,6 +644,7 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
     }
     s.num_parts = go ? np : -1;
     s.epoch = ep;
+    s.spin_limit = sl;
   }
   {   // counts (into prefix, scanned below) and offsets of the three lists
     constexpr int kEntries = 3 * kMaxParts;

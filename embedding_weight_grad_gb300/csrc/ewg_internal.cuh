@@ -107,9 +107,19 @@ struct Header {
   int work[2];           // next work item of the apply kernel (zeroed by the plan)
   int done;              // apply CTAs that have finished (zeroed by the plan)
   int epoch;             // apply calls completed on this plan (zeroed by the plan)
-  int pad[53];
+  int spin_limit;        // polls of a fold's arrival counter before it gives up (set by
+                         // the plan to kFoldSpinLimit)
+  int pad[52];
 };
 static_assert(sizeof(Header) == 256, "header is one 256-byte region");
+// The GPU tests of the timeout path overwrite these two fields between ewg_plan and
+// ewg_apply (an unreachable epoch and a short limit), so their offsets are fixed.
+static_assert(offsetof(Header, epoch) == 40 && offsetof(Header, spin_limit) == 44,
+              "header offsets the timeout tests rely on");
+
+// Default bound on the polls of a fold's arrival counter (each poll is an L2 round trip
+// plus a short sleep: a few seconds in all, far beyond any legitimate wait).
+constexpr int kFoldSpinLimit = 1 << 22;
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

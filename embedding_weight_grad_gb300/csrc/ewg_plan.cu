@@ -275,6 +275,7 @@ __device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
   h->work[0] = h->work[1] = 0;
   h->done = 0;
   h->epoch = 0;
+  h->spin_limit = kFoldSpinLimit;
   h->status = bad ? EWG_ERR_ID_OUT_OF_RANGE : EWG_OK;
 }
 

@@ -5,9 +5,11 @@
 // and runtimes that forbid cudaMalloc after start-up.  For them this file owns a fixed
 // block of device memory, a file-scope __device__ array, and uses it as the workspace of
 // ewg_accumulate.  The block is reserved on every device that loads the library and kept
-// until the process exits.  Calls are limited to sizes whose workspace fits in it.  The
-// first call on a device looks up the block's device address (make it outside any
-// stream capture); calls that overlap on the GPU race on the block.
+// until the process exits (under CUDA's default lazy module loading, from the first
+// call on the device, whose address lookup loads this module).  Calls are limited to
+// sizes whose workspace fits in it.  The first call on a device looks up the block's
+// device address (make it at start-up, outside any stream capture); calls that overlap
+// on the GPU race on the block.
 #include <mutex>
 
 #include "ewg.h"

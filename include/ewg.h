@@ -97,7 +97,9 @@ int ewg_can_accumulate(const void* ids, int ids_dtype, int64_t num_tokens,
 
 /*
  * Bytes of device workspace that ewg_accumulate / ewg_plan / ewg_apply need for
- * num_tokens tokens of width hidden (an upper bound over every id pattern).  The
+ * num_tokens tokens of width hidden (an upper bound over every id pattern).  The page
+ * has no counterpart: its function allocates its own scratch, while this library leaves
+ * every allocation to the caller.  The
  * workspace needs no initialisation and holds no state the caller must keep
  * between calls, except that ewg_apply reads the plan that ewg_plan left in it and
  * ewg_read_status reads the status of the last call.  Returns 0 for sizes outside
@@ -198,6 +200,14 @@ int ewg_plan_shard(const void* ids, int ids_dtype, int64_t num_tokens,
  * work already queued on `stream`); the apply waits for both.  Calls on one device from
  * several host threads are serialised by the library while they enqueue.  Errors and
  * the device status: as ewg_accumulate (ewg_read_status on the same workspace).
+ *
+ * The copies read ids_host and grad_host after the call has returned: both buffers must
+ * stay allocated and unchanged until `stream` has passed this call (synchronize it, or
+ * wait on an event recorded on it after the call).
+ *
+ * The library keeps ONE copy stream per device for every caller stream, so the grad
+ * copy of a call waits for the grad copies of earlier host-input calls on the same
+ * device, whatever stream those were made on.
  */
 size_t ewg_host_workspace_bytes(int64_t num_tokens, int64_t hidden, int ids_dtype,
                                 int grad_dtype);
@@ -211,8 +221,9 @@ int ewg_accumulate_host(const void* ids_host, int ids_dtype, int64_t num_tokens,
 #define EWG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /*
- * ewg_accumulate without a caller workspace and without any allocation.  (The paper
- * has no counterpart; this is an addition for callers that cannot allocate.)
+ * ewg_accumulate without a caller workspace and without any allocation.  Neither the
+ * page nor the paper behind it has a counterpart: this is an addition for callers that
+ * cannot allocate.
  *
  * For callers that cannot allocate device memory when the gradient is accumulated:
  * code running under a fixed-pool or custom allocator that must not grow, and runtimes
@@ -227,7 +238,10 @@ int ewg_accumulate_host(const void* ids_host, int ids_dtype, int64_t num_tokens,
  *   tokens for hidden sizes up to about 10000.
  * - The call makes no cudaMalloc, cudaFree or other allocating call.  The first call on
  *   a device looks up the array's device address with cudaGetSymbolAddress; make that
- *   first call outside any stream capture.
+ *   first call outside any stream capture.  Under CUDA's lazy module loading (the
+ *   default) the array is reserved only then, when that lookup loads the module that
+ *   holds it (with CUDA_MODULE_LOADING=EAGER, when the library is loaded): make the
+ *   first call at start-up, while the device still has room for it.
  * - Every call on a device uses the same array, which keeps the last call's contents
  *   (nothing in it needs clearing between calls).  Calls that may overlap on the GPU
  *   (different streams without ordering) race on it and must not be made.
@@ -244,7 +258,9 @@ int ewg_accumulate_static(const void* ids, int ids_dtype, int64_t num_tokens,
  * Waits for `stream`, then copies the device status of the last ewg_plan /
  * ewg_apply / ewg_accumulate that used this workspace into *status (EWG_OK,
  * EWG_ERR_ID_OUT_OF_RANGE, EWG_ERR_INVALID or EWG_ERR_TIMEOUT).  Returns EWG_OK or
- * EWG_ERR_CUDA.
+ * EWG_ERR_CUDA.  The page has no counterpart: there an out-of-range id stops the
+ * process with a device assertion, while here it is reported through this call (the
+ * device-status query of the library's boundary).
  */
 int ewg_read_status(const void* workspace, void* stream, int* status);
 

@@ -74,7 +74,9 @@ float load_elem(const void* base, int dtype, int64_t index) {
   return static_cast<const float*>(base)[index];
 }
 
-// "rounds once to the gradient dtype": returns the rounded value as a float
+// The single rounding of a token's summed row to the gradient's dtype (Megatron Core API
+// docs, core.fusions.fused_embedding_wgrad, module docstring, first bullet); returns the
+// rounded value widened back to float.
 float round_to(int dtype, float x) {
   if (dtype == kBf16) return bf16_to_float(float_to_bf16(x));
   return x;  // fp32 -> fp32 is the identity
@@ -134,7 +136,9 @@ struct GradView {
 void run_weight_grad(const Run& run, const std::vector<int64_t>& sorted_pos,
                      const GradView& g, int64_t H, std::vector<float>& total,
                      std::vector<float>& part, float* w_out) {
-  total.assign(H, 0.0f);  // "adds the partial sums in order starting from 0"
+  // the partial sums are combined in chunk order, beginning from zero (module docstring,
+  // first bullet)
+  total.assign(H, 0.0f);
   for (int64_t c0 = 0; c0 < run.length; c0 += kNrows) {
     const int64_t c1 = std::min<int64_t>(c0 + kNrows, run.length);
     part.assign(H, 0.0f);  // each partial sum starts at +0

@@ -245,6 +245,35 @@ def test_unsupported_inputs_are_rejected_before_any_work():
     assert not ewg.can_accumulate_embedding_wgrad(ids_d, wide[:, 1:257], mg)
 
 
+def test_tensors_overlapping_the_workspace_are_rejected():
+    """One allocation carved into the workspace and main_grad (or grad) so that they share
+    bytes: every entry point that writes the workspace must refuse before any work."""
+    ids, grad, mg = make(4000, 1000, 256, seed=52)
+    ids_d = torch.from_numpy(ids).to(DEV)
+    need = ewg.workspace_bytes(4000, 256)
+    L = ewg.lib()
+    stream = torch.cuda.current_stream().cuda_stream
+    buf = torch.zeros(need + max(mg.numel() * 4, grad.numel() * 2), dtype=torch.uint8, device=DEV)
+    ws = buf[:need]
+    # main_grad starts inside the workspace (256-byte aligned, half way in)
+    mg_in = buf[need // 512 * 256:].view(torch.float32)[: mg.numel()].view(mg.shape)
+    mg_in.copy_(mg)
+    before = mg_in.clone()
+    a = ewg._Args(ids_d, grad, mg_in)
+    code = L.ewg_accumulate(*a.c_args(), ws.data_ptr(), need, stream)
+    assert code == ewg.ERR_UNSUPPORTED and b"overlaps the workspace" in L.ewg_last_error()
+    code = L.ewg_apply(grad.data_ptr(), ewg._BF16, 256, mg_in.data_ptr(), ewg._FP32, 4000, 1000,
+                       256, 256, ws.data_ptr(), need, stream)
+    assert code == ewg.ERR_UNSUPPORTED and b"overlaps the workspace" in L.ewg_last_error()
+    # grad inside the workspace
+    g_in = buf[need // 512 * 256:].view(torch.bfloat16)[: grad.numel()].view(grad.shape)
+    b = ewg._Args(ids_d, g_in, mg)
+    code = L.ewg_accumulate(*b.c_args(), ws.data_ptr(), need, stream)
+    assert code == ewg.ERR_UNSUPPORTED and b"overlaps the workspace" in L.ewg_last_error()
+    torch.cuda.synchronize()
+    assert_same_bits(mg_in, before)
+
+
 def test_deterministic_across_runs(oracle_mod):
     w = workloads.scaled(workloads.BY_NAME["long_runs"], hidden=512)
     ids = workloads.make_ids(w)

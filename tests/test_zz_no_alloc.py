@@ -70,6 +70,22 @@ def test_static_matches_workspace_entry_point_twice(lib, name):
         assert same_bits(mg_static, mg_ref)
 
 
+def test_static_call_allocates_nothing(lib):
+    """After a first call on the device (which may load the module that holds the array),
+    further calls leave the device's free memory exactly as it was."""
+    w = workloads.BY_NAME["gpt2_like"]
+    ids = torch.from_numpy(workloads.make_ids(w).reshape(-1)).to(DEV)
+    grad = workloads.make_grad(w, DEV).reshape(ids.numel(), w.hidden)
+    mg = workloads.make_main_grad(w, DEV)
+    assert call_static(lib, ids, grad, mg) == ewg.OK, lib.ewg_last_error()
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info(DEV)[0]
+    for _ in range(3):
+        assert call_static(lib, ids, grad, mg) == ewg.OK, lib.ewg_last_error()
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info(DEV)[0] == free_before
+
+
 def test_static_rejects_sizes_beyond_its_scratch(lib):
     w = workloads.scaled(workloads.BY_NAME["long_runs"], num_embeddings=1000)
     n, H = 65536, 7168
