@@ -200,13 +200,13 @@ def kernel_source_hash():
 
 def kernel_launches_per_call(n, V):
     """Kernels one accumulate call launches: the plan (one hashed kernel up to 8192
-    tokens; otherwise pack, per radix pass a scan and a scatter plus a histogram after the
-    first, then three listing kernels) and the apply kernel."""
+    tokens; otherwise pack, a digit histogram, one sweep per radix pass of at most 9 id
+    bits, and the listing) and the apply kernel."""
     if n <= 8192:
         return 1 + 1
     id_bits = max(0, int(V - 1).bit_length())
     passes = -(-id_bits // 9)
-    return 1 + 2 * passes + max(0, passes - 1) + 3 + 1
+    return 1 + (1 if passes else 0) + passes + 1 + 1
 
 
 def time_events(fn, steps, stream, flush):
@@ -284,6 +284,28 @@ def run_ours(args, w, world, rank, local):
     # written back inside the timed call
     per_call_clean = time_events(call, args.steps, stream, flush_clean)
 
+    # calls enqueued back to back (no flush, no host synchronisation in between): the GPU
+    # never idles, and each call finds L2 as the previous call left it
+    per_call_b2b = time_events(call, args.steps, stream, lambda: None)
+
+    # calls made after the GPU has sat idle: the host synchronises and waits 1 ms before
+    # each call.  An idle GB300 runs the next few tens of microseconds slower (a GPU-side
+    # sleep kernel of 50 us or more before the call, which touches no memory, removes the
+    # difference), so this is a property of the idle GPU, not of the call.
+    def idle():
+        torch.cuda.synchronize()
+        time.sleep(1e-3)
+
+    idle_evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(max(10, args.steps // 10))]
+    for s_ev, e_ev in idle_evs:
+        idle()
+        s_ev.record(stream)
+        call()
+        e_ev.record(stream)
+    torch.cuda.synchronize()
+    per_call_idle = [s_ev.elapsed_time(e_ev) for s_ev, e_ev in idle_evs]
+
     # the same call split into its two C-ABI halves, to time the apply kernel alone
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     for e0, e1, e2 in ev:
@@ -317,9 +339,10 @@ def run_ours(args, w, world, rank, local):
     sampler.mark()
     sampler.stop()
 
-    mean_ms, median_ms, plan_mean, apply_mean, e2e_mean, clean_ms = reduce_max(
+    mean_ms, median_ms, plan_mean, apply_mean, e2e_mean, clean_ms, b2b_ms, idle_ms = reduce_max(
         [statistics.fmean(per_call), statistics.median(per_call), statistics.fmean(plan_ms),
-         statistics.fmean(apply_ms), statistics.fmean(e2e_ms), statistics.fmean(per_call_clean)],
+         statistics.fmean(apply_ms), statistics.fmean(e2e_ms), statistics.fmean(per_call_clean),
+         statistics.fmean(per_call_b2b), statistics.fmean(per_call_idle)],
         world, dev)
 
     out = None
@@ -358,6 +381,10 @@ def run_ours(args, w, world, rank, local):
             "plan_us": round(plan_mean * 1e3, 3),
             "clean_l2": {"value": round(clean_ms * 1e3, 3), "unit": "us/call",
                          "flush": "256 MiB memset then a 256 MiB read before every call"},
+            "back_to_back": {"value": round(b2b_ms * 1e3, 3), "unit": "us/call",
+                             "what": "calls enqueued with no flush and no host sync in between"},
+            "after_idle": {"value": round(idle_ms * 1e3, 3), "unit": "us/call",
+                           "what": "host sync and 1 ms of GPU idle before every call"},
             "apply_us": round(apply_mean * 1e3, 3),
             "roofline": {
                 "kernel": "apply_kernel (one ewg_apply call)",

@@ -30,11 +30,15 @@ MAX_TOKENS = 1 << 28
 NROWS = 10
 
 _INT32, _INT64, _BF16, _FP32 = 0, 1, 2, 3
-OK, ERR_UNSUPPORTED, ERR_INVALID, ERR_CUDA, ERR_ID_OUT_OF_RANGE, ERR_TIMEOUT = 0, 1, 2, 3, 4, 5
+OK, ERR_UNSUPPORTED, ERR_INVALID, ERR_CUDA, ERR_ID_OUT_OF_RANGE, ERR_TIMEOUT, ERR_BOUNDS = \
+    0, 1, 2, 3, 4, 5, 6
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libewg.so")
+# The same library built with every kernel index checked (EWG_ERR_BOUNDS on a failure).
+_DEBUG_LIB_PATH = os.path.join(_HERE, "libewg_debug.so")
 _lib = None
+_debug_lib = None
 _lock = threading.Lock()
 # Pinned host tensors handed to the host-input call, each kept alive until an event
 # recorded after the call has completed: the library copies from their raw pointers, so
@@ -60,43 +64,57 @@ def lib():
         return _lib
     with _lock:
         if _lib is None:
-            if not os.path.exists(_LIB_PATH):
-                raise ImportError(
-                    f"{_LIB_PATH} is missing: build it with "
-                    "`python -m embedding_weight_grad_gb300.build` (needs nvcc)")
-            L = ctypes.CDLL(_LIB_PATH)
-            i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
-            L.ewg_can_accumulate.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64]
-            L.ewg_can_accumulate.restype = i32
-            L.ewg_workspace_bytes.argtypes = [i64, i64]
-            L.ewg_workspace_bytes.restype = sz
-            L.ewg_accumulate.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64, vp,
-                                         sz, vp]
-            L.ewg_accumulate.restype = i32
-            L.ewg_plan.argtypes = [vp, i32, i64, i64, i64, vp, sz, vp]
-            L.ewg_plan.restype = i32
-            L.ewg_apply.argtypes = [vp, i32, i64, vp, i32, i64, i64, i64, i64, vp, sz, vp]
-            L.ewg_apply.restype = i32
-            L.ewg_accumulate_shard.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64,
-                                               i64, i64, vp, sz, vp]
-            L.ewg_accumulate_shard.restype = i32
-            L.ewg_plan_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, sz, vp]
-            L.ewg_plan_shard.restype = i32
-            L.ewg_host_workspace_bytes.argtypes = [i64, i64, i32, i32]
-            L.ewg_host_workspace_bytes.restype = sz
-            L.ewg_accumulate_host.argtypes = [vp, i32, i64, vp, i32, vp, i32, i64, i64, i64, vp,
-                                              sz, vp]
-            L.ewg_accumulate_host.restype = i32
-            L.ewg_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
-            L.ewg_read_status.restype = i32
-            L.ewg_status_string.argtypes = [i32]
-            L.ewg_status_string.restype = ctypes.c_char_p
-            L.ewg_last_error.argtypes = []
-            L.ewg_last_error.restype = ctypes.c_char_p
-            L.ewg_version.argtypes = []
-            L.ewg_version.restype = i32
-            _lib = L
+            _lib = _load(_LIB_PATH)
     return _lib
+
+
+def debug_lib():
+    """The bounds-checking build of the same library (libewg_debug.so), for tests."""
+    global _debug_lib
+    if _debug_lib is not None:
+        return _debug_lib
+    with _lock:
+        if _debug_lib is None:
+            _debug_lib = _load(_DEBUG_LIB_PATH)
+    return _debug_lib
+
+
+def _load(path):
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m embedding_weight_grad_gb300.build` (needs nvcc)")
+    L = ctypes.CDLL(path)
+    i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    L.ewg_can_accumulate.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64]
+    L.ewg_can_accumulate.restype = i32
+    L.ewg_workspace_bytes.argtypes = [i64, i64]
+    L.ewg_workspace_bytes.restype = sz
+    L.ewg_accumulate.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64, vp,
+                                 sz, vp]
+    L.ewg_accumulate.restype = i32
+    L.ewg_plan.argtypes = [vp, i32, i64, i64, i64, vp, sz, vp]
+    L.ewg_plan.restype = i32
+    L.ewg_apply.argtypes = [vp, i32, i64, vp, i32, i64, i64, i64, i64, vp, sz, vp]
+    L.ewg_apply.restype = i32
+    L.ewg_accumulate_shard.argtypes = [vp, i32, i64, vp, i32, i64, vp, i32, i64, i64, i64,
+                                       i64, i64, vp, sz, vp]
+    L.ewg_accumulate_shard.restype = i32
+    L.ewg_plan_shard.argtypes = [vp, i32, i64, i64, i64, i64, i64, vp, sz, vp]
+    L.ewg_plan_shard.restype = i32
+    L.ewg_host_workspace_bytes.argtypes = [i64, i64, i32, i32]
+    L.ewg_host_workspace_bytes.restype = sz
+    L.ewg_accumulate_host.argtypes = [vp, i32, i64, vp, i32, vp, i32, i64, i64, i64, vp,
+                                      sz, vp]
+    L.ewg_accumulate_host.restype = i32
+    L.ewg_read_status.argtypes = [vp, vp, ctypes.POINTER(i32)]
+    L.ewg_read_status.restype = i32
+    L.ewg_status_string.argtypes = [i32]
+    L.ewg_status_string.restype = ctypes.c_char_p
+    L.ewg_last_error.argtypes = []
+    L.ewg_last_error.restype = ctypes.c_char_p
+    L.ewg_version.argtypes = []
+    L.ewg_version.restype = i32
+    return L
 
 
 def _raise_on(code: int):

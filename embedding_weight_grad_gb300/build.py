@@ -16,6 +16,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libewg.so")
+# The same sources with EWG_DEBUG: every index a kernel derives from the plan is checked,
+# and a failed check sets EWG_ERR_BOUNDS instead of making the access.
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libewg_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -40,15 +44,16 @@ def _newest_input():
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    lib, out_dir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags)
+    flags = NVCC_FLAGS + list(extra_flags) + (["-DEWG_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -59,14 +64,21 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([cc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(force: bool = False) -> None:
+    """The library and its bounds-checking twin, both compiled in parallel."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        list(ex.map(lambda d: build(force=force, debug=d), (False, True)))
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
-    print(build(force="-f" in sys.argv, verbose=v, extra_flags=["-Xptxas", "-v"] if v else []))
+    print(build(force="-f" in sys.argv, verbose=v, extra_flags=["-Xptxas", "-v"] if v else [],
+                debug="--debug" in sys.argv))

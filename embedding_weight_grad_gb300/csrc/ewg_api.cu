@@ -194,10 +194,16 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t row_be
   a.keys_b = at<uint32_t>(ws, L.keys_b);
   a.vals_b = at<uint32_t>(ws, L.vals_b);
   a.chunks = at<int>(ws, L.chunks);
+  a.chunk_cap = static_cast<int>(L.short_base + n);
+  a.run_cap = static_cast<int>(ewg::max_long_runs(n));
+  a.partial_cap = static_cast<int>(ewg::max_partial_rows(n));
+  a.short_base = static_cast<int>(L.short_base);
   a.runs = at<int>(ws, L.runs);
-  a.hist = at<uint32_t>(ws, L.hist);
+  a.sweep = at<uint32_t>(ws, L.sweep);
+  a.totals = at<uint32_t>(ws, L.ctl);
+  a.counters = a.totals + ewg::kMaxPasses * (1 << ewg::kMaxDigitBits);
   a.tile_bad = at<int>(ws, L.tile_bad);
-  a.tile_cnt = at<int4>(ws, L.tile_cnt);
+  a.list_status = at<uint32_t>(ws, L.list_status);
   a.arrivals = at<int>(ws, L.arrivals);
   cudaError_t e = ewg::launch_plan(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "plan launch");
@@ -224,6 +230,7 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.chunks = at<int>(ws, L.chunks);
   a.runs = at<int>(ws, L.runs);
   a.partial = at<float>(ws, L.partial);
+  a.partial_cap = static_cast<int>(ewg::max_partial_rows(n));
   a.arrivals = at<int>(ws, L.arrivals);
   // Only when the plan of the same call runs just before (and every grad row is read):
   // up to kPrefetchBytes of the first grad rows, at most half of them.
@@ -423,6 +430,7 @@ const char* ewg_status_string(int status) {
     case EWG_ERR_CUDA: return "EWG_ERR_CUDA";
     case EWG_ERR_ID_OUT_OF_RANGE: return "EWG_ERR_ID_OUT_OF_RANGE";
     case EWG_ERR_TIMEOUT: return "EWG_ERR_TIMEOUT";
+    case EWG_ERR_BOUNDS: return "EWG_ERR_BOUNDS";
     default: return "EWG_ERR_UNKNOWN";
   }
 }

@@ -256,14 +256,20 @@ struct Producer {
     const int col0 = tile * tc;
     const int cols = min(tc, a.hidden - col0);
     const int meta = d[kDescMeta];
-    const int len = meta & 15;
-    const int id = d[kDescId];
+    int len = meta & 15;
+    int id = d[kDescId];
+    int prow = d[kDescPartial], C = d[kDescNumChunks], ci = meta >> 4;
+    if (!checked(len >= 1 && len <= kNrows, a.header)) len = 1;
+    if (!checked(is_long || (id >= 0 && id < a.num_embeddings), a.header)) id = 0;
+    if (!checked(!is_long || (C >= 1 && ci < C && prow - ci >= 0 && prow - ci + C <= a.partial_cap), a.header))
+      prow = ci = 0, C = 1;
     const uint32_t row_bytes = cols * (GBF16 ? 2 : 4);
     const uint32_t mg_bytes = is_long ? 0u : cols * (MBF16 ? 2 : 4);
     const uint32_t bytes = len * row_bytes + mg_bytes;
     const char* src = nullptr;   // this lane's segment: grad row `lane`, or the main_grad row
     if (lane < len) {
-      const long long p = d[kDescPos + lane];
+      long long p = d[kDescPos + lane];
+      if (!checked(p >= 0 && p < a.n, a.header)) p = 0;
       src = static_cast<const char*>(a.grad) + (p * a.grad_stride + col0) * (GBF16 ? 2 : 4);
     } else if (lane == len && !is_long) {
       src = static_cast<const char*>(a.main_grad) +
@@ -276,8 +282,8 @@ struct Producer {
     const int off = reserve(bytes);
     if (off < 0) return false;
     // for a long chunk, flags holds its index c in the run (prow - c: the run's counter)
-    Item it{off, len, is_long ? d[kDescNumChunks] : id, d[kDescPartial], col0, cols,
-            is_long ? kLongChunk : kShortChunk, is_long ? (meta >> 4) : 0};
+    Item it{off, len, is_long ? C : id, prow, col0, cols, is_long ? kLongChunk : kShortChunk,
+            is_long ? ci : 0};
     uint64_t* bar = open(it, bytes);
     if (src) ptx::bulk_g2s(ring + off + lane * row_bytes, src, src_bytes, bar, pol);
     return true;
@@ -319,6 +325,10 @@ struct Producer {
   __device__ bool combine_task(const int* run, int group, int Tl) {
     const int prow0 = run[0], C = run[1], id = run[2];
     const int split = run[3] >> 4, width = kCombineCols / split;
+    if (!checked(prow0 >= 0 && C >= 1 && prow0 + C <= a.partial_cap && id >= 0 && id < a.num_embeddings &&
+                     (split == 1 || split == 2 || split == 4) && (run[3] & 15) < split,
+                 a.header))
+      return true;   // nothing is issued for a fold whose table entry is out of range
     const int col0 = group * kCombineCols + (run[3] & 15) * width;
     const int cols = min(width, a.hidden - col0);
     if (cols <= 0) return true;   // a slice past the last column: nothing to fold

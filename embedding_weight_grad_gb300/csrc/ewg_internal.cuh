@@ -60,6 +60,7 @@ constexpr int kMaxDigitBits = 9;                          // 512 buckets per rad
 constexpr int kTileThreads = 256;
 constexpr int kTileItems = 8;
 constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
+constexpr int kMaxPasses = 4;                             // ids below 2^31: 31 bits, 9 per pass
 
 // Apply kernel.  Bulk copies reach full HBM bandwidth only from about 4 KB up, so an
 // item covers a chunk over a column tile of up to 2048 columns (1024 for an fp32
@@ -95,7 +96,7 @@ inline int tile_cols(int64_t hidden, bool grad_bf16, bool long_chunks) {
   return static_cast<int>((per + 7) / 8 * 8);
 }
 
-enum DeviceStatus { kStatusOk = 0, kStatusInvalid = 2, kStatusBadId = 4, kStatusTimeout = 5 };
+enum DeviceStatus { kStatusOk = 0, kStatusInvalid = 2, kStatusBadId = 4, kStatusTimeout = 5, kStatusBounds = 6 };
 
 struct Header {
   int status;            // EWG_OK or the device-detected error of the last call
@@ -121,6 +122,19 @@ static_assert(offsetof(Header, epoch) == 40 && offsetof(Header, spin_limit) == 4
 // plus a short sleep: a few seconds in all, far beyond any legitimate wait).
 constexpr int kFoldSpinLimit = 1 << 22;
 
+// Index checks of the bounds-checking build (compiled with EWG_DEBUG): returns `ok`, and
+// a false one records EWG_ERR_BOUNDS in the status word, after which the caller replaces
+// the access by a safe one (row or slot 0).  In the ordinary build every index is
+// trusted and the check compiles to nothing.
+#ifdef EWG_DEBUG
+__device__ __forceinline__ bool checked(bool ok, const Header* h) {
+  if (!ok) atomicExch(const_cast<int*>(&h->status), kStatusBounds);
+  return ok;
+}
+#else
+__device__ __forceinline__ bool checked(bool, const Header*) { return true; }
+#endif
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -142,9 +156,10 @@ inline int64_t max_partial_rows(int64_t n) { return 2 * n / 11 + kMaxParts + 1; 
 inline int64_t max_long_runs(int64_t n) { return n / 11 + n / 100 + kMaxParts + 1; }
 
 struct Layout {
-  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, hist, tile_bad, tile_cnt, arrivals,
-      partial, total;
+  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, sweep, ctl, tile_bad, list_status,
+      arrivals, partial, total;
   int64_t n, hidden, tiles;
+  int64_t short_base;   // multi-tile plan: descriptor index of the first short chunk
 };
 
 inline Layout make_layout(int64_t n, int64_t hidden) {
@@ -165,11 +180,15 @@ inline Layout make_layout(int64_t n, int64_t hidden) {
   L.vals_a = take(n_pad * 4);
   L.keys_b = take(n_pad * 4);
   L.vals_b = take(n_pad * 4);
-  L.chunks = take(static_cast<size_t>(n) * kChunkWords * 4);
+  // Chunk descriptors.  The hashed plan uses the first n; the multi-tile plan puts the long
+  // runs' chunks first (at most max_partial_rows(n) of them) and the short chunks after.
+  L.short_base = max_partial_rows(n);
+  L.chunks = take(static_cast<size_t>(L.short_base + n) * kChunkWords * 4);
   L.runs = take(static_cast<size_t>(max_long_runs(n)) * kRunWords * 4);
-  L.hist = take(static_cast<size_t>(L.tiles) * (1 << kMaxDigitBits) * 4);
+  L.sweep = take(static_cast<size_t>(kMaxPasses) * L.tiles * (1 << kMaxDigitBits) * 4);
+  L.ctl = take(static_cast<size_t>(kMaxPasses * (1 << kMaxDigitBits) + kMaxPasses + 1) * 4);
   L.tile_bad = take(static_cast<size_t>(L.tiles) * 4);
-  L.tile_cnt = take(static_cast<size_t>(L.tiles) * 16);
+  L.list_status = take(static_cast<size_t>(L.tiles) * 16);
   L.arrivals = take(static_cast<size_t>(max_partial_rows(n)) * 4);
   L.partial = take(static_cast<size_t>(max_partial_rows(n)) * partial_row_floats(hidden) * 4);
   L.total = off;
@@ -220,10 +239,16 @@ struct PlanArgs {
   uint32_t* keys_b;
   uint32_t* vals_b;
   int* chunks;
+  int chunk_cap;         // descriptors, long-run table entries and partial rows the
+  int run_cap;           // workspace holds (checked by the bounds-checking build)
+  int partial_cap;
+  int short_base;        // multi-tile plan: descriptor index of the first short chunk
   int* runs;
-  uint32_t* hist;
-  int* tile_bad;
-  int4* tile_cnt;        // per tile: long chunks, short chunks, long runs
+  uint32_t* sweep;       // [pass][tile][bucket] look-back words of the radix sweeps
+  uint32_t* totals;      // [pass][bucket] keys per digit over all tiles
+  uint32_t* counters;    // [pass] tiles claimed by each sweep, [kMaxPasses] by the listing
+  int* tile_bad;         // per tile: ids outside [0, num_embeddings)
+  uint32_t* list_status; // per tile, 4 words: look-back words of long chunks, short chunks, long runs
   int* arrivals;         // per long run, at its first partial row: zeroed here
 };
 
@@ -242,6 +267,7 @@ struct ApplyArgs {
   const int* chunks;
   const int* runs;
   float* partial;
+  int partial_cap;         // partial rows the workspace holds
   int* arrivals;           // per long run (at its first partial row): finished chunk parts
   int prefetch_rows;       // grad rows [0, prefetch_rows) pulled into L2 before the kernel
                            // waits on the plan (0: none)

@@ -15,8 +15,10 @@
 //
 // Above 8192 tokens (multi-tile path): an LSD radix sort over the id bits only (keys
 // arrive in position order and every pass is stable, so positions stay ascending in
-// each run without passes of their own) as histogram / scan / scatter kernels over
-// tiles of 2048 keys, then count / scan / emit kernels for the listing.
+// each run without passes of their own) over tiles of 2048 keys, one kernel per pass:
+// each tile ranks its keys and finds where its digits start by decoupled look-back over
+// the tiles before it (a single sweep per pass, in the manner of a "onesweep" radix
+// sort), then one listing kernel that places its chunks by the same look-back.
 //
 // The listing gives every sorted slot s its run's first slot rs and last slot re.
 // Slot s starts a chunk when (s - rs) % NROWS == 0.
@@ -240,10 +242,17 @@ struct Listing {
       const bool is_long = L > kNrows;
       const int desc = is_long ? b.long_desc + li : b.short_desc + si;
       const int prow = is_long ? b.partial + li : -1;
+      if (!checked(desc >= 0 && desc < a.chunk_cap && prow < a.partial_cap &&
+                       (!is_long || c != 0 || b.run + ri + fold_entries(C) <= a.run_cap),
+                   a.header))
+        continue;
       int4* d = reinterpret_cast<int4*>(a.chunks + static_cast<long long>(desc) * kChunkWords);
       int p[kNrows];
 #pragma unroll
-      for (int k = 0; k < kNrows; ++k) p[k] = k < len ? static_cast<int>(vals[s + k]) : 0;
+      for (int k = 0; k < kNrows; ++k) {
+        p[k] = k < len ? static_cast<int>(vals[s + k]) : 0;
+        if (!checked(p[k] >= 0 && p[k] < n, a.header)) p[k] = 0;
+      }
       d[0] = make_int4(p[0], p[1], p[2], p[3]);
       d[1] = make_int4(p[4], p[5], p[6], p[7]);
       d[2] = make_int4(p[8], p[9], static_cast<int>(key[i]), len | (c << 4));
@@ -265,7 +274,9 @@ struct Listing {
   }
 };
 
-__device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
+// Everything of the header but its status word: the plan's stamp and the apply kernel's
+// counters.
+__device__ void write_header_fields(const PlanArgs& a, int num_parts, int bad) {
   Header* h = a.header;
   h->n = a.n;
   h->hidden = a.hidden;
@@ -276,7 +287,11 @@ __device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
   h->done = 0;
   h->epoch = 0;
   h->spin_limit = kFoldSpinLimit;
-  h->status = bad ? EWG_ERR_ID_OUT_OF_RANGE : EWG_OK;
+}
+
+__device__ void write_header(const PlanArgs& a, int num_parts, int bad) {
+  write_header_fields(a, num_parts, bad);
+  a.header->status = bad ? EWG_ERR_ID_OUT_OF_RANGE : EWG_OK;
 }
 
 __device__ void write_tables(const PlanArgs& a, int part, int long_cnt, int long_off,
@@ -480,10 +495,12 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
         const int C = (L + kNrows - 1) / kNrows;
         tbase[s] = static_cast<uint32_t>(long_desc + li);
         const int split = fold_entries(C);
-        for (int q = 0; q < split; ++q)
-          reinterpret_cast<int4*>(a.runs)[run_base + ri + q] =
-              make_int4(partial_base + li, C, static_cast<int>(tkey[s]), q | (split << 4));
-        a.arrivals[partial_base + li] = 0;
+        if (checked(run_base + ri + split <= a.run_cap && partial_base + li + C <= a.partial_cap, a.header)) {
+          for (int q = 0; q < split; ++q)
+            reinterpret_cast<int4*>(a.runs)[run_base + ri + q] =
+                make_int4(partial_base + li, C, static_cast<int>(tkey[s]), q | (split << 4));
+          a.arrivals[partial_base + li] = 0;
+        }
         li += C;
         ri += split;
       } else if (L > 0) {
@@ -503,6 +520,7 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
     const int L = static_cast<int>(tcnt[s]);
     const int c = r / kNrows, k = r - c * kNrows;
     const int desc = static_cast<int>(tbase[s]) + c;
+    if (!checked(desc >= 0 && desc < a.chunk_cap && kpos[i] < static_cast<uint32_t>(a.n), a.header)) continue;
     int* d = a.chunks + static_cast<long long>(desc) * kChunkWords;
     d[kDescPos + k] = static_cast<int>(kpos[i]);
     if (k == 0) {
@@ -522,17 +540,87 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
 
 // ---------------------------------------------------------------------------
 // Multi-tile plan: tiles of kTile keys, one CTA each.
+//
+//   pack    each tile's keys (the id, or a skip / pad key) and positions; counts its bad
+//           ids; clears what the later kernels count into
+//   hist    digit histograms of every radix pass over all keys (global atomics)
+//   sweep   one per radix pass: a stable scatter in which each tile ranks its keys by
+//           digit, publishes its digit counts and sums the counts of the tiles before it
+//           by decoupled look-back.  Tiles are taken in claim order from a counter, so
+//           the tiles before a running one are running or done and every wait ends.
+//   list    runs and chunks of the sorted keys: each tile counts its chunks and runs,
+//           sums the counts of the tiles before it by the same look-back, and writes its
+//           descriptors; the last tile writes the tables and the header.
+// Every look-back poll is bounded; a tile that gives up sets EWG_ERR_TIMEOUT and the
+// kernels after it write nothing.
 
-// Keys of the tile into the ping buffer, plus the pass-0 digit histogram.
-__global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
-  __shared__ uint32_t h[1 << kMaxDigitBits];
+constexpr uint32_t kFlagAgg = 1u << 30;   // the word holds the tile's own count
+constexpr uint32_t kFlagInc = 2u << 30;   // ... the sum over the tile and all before it
+constexpr uint32_t kCountMask = kFlagAgg - 1u;
+constexpr int kLookBackPolls = 1 << 20;   // polls of one predecessor's word (about 0.5 s)
+
+__device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Look-back over NCH chains of words at once (chain c: tile j's word at word[c] + j *
+// stride).  This tile has published its own counts as aggregates (or, as tile 0, as
+// inclusive sums).  Each round loads the words of the K closest predecessors not yet
+// summed, all in flight together, then adds them from the closest one on until a word
+// holds an inclusive sum; since every tile publishes its aggregate early, a round
+// usually settles a chain of up to K tiles in one round trip.  Publishes this tile's
+// inclusive sums.  False if a predecessor published nothing within the poll limit.
+template <int K, int NCH>
+__device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int tile, const bool (&active)[NCH],
+                          const uint32_t (&own)[NCH], uint32_t (&excl)[NCH]) {
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    if (!active[c]) continue;
+    uint32_t sum = 0;
+    for (int hi = tile; hi > 0;) {
+      const int m = min(hi, K);
+      uint32_t v[K];
+#pragma unroll
+      for (int i = 0; i < K; ++i) v[i] = i < m ? ld_relaxed(word[c] + (hi - 1 - i) * stride) : kFlagInc;
+      bool stop = false;
+#pragma unroll
+      for (int i = 0; i < K; ++i) {
+        if (i >= m || stop) continue;
+        for (int p = 0; p < kLookBackPolls && !(v[i] & ~kCountMask); ++p) {
+          __nanosleep(32);
+          v[i] = ld_relaxed(word[c] + (hi - 1 - i) * stride);
+        }
+        if (!(v[i] & ~kCountMask)) return false;
+        sum += v[i] & kCountMask;
+        stop = (v[i] & kFlagInc) != 0;
+      }
+      if (stop) break;
+      hi -= m;
+    }
+    st_relaxed(word[c] + tile * stride, kFlagInc | (sum + own[c]));
+    excl[c] = sum;
+  }
+  return true;
+}
+
+__device__ void give_up_plan(const PlanArgs& a) { atomicExch(&a.header->status, kStatusTimeout); }
+
+// Digit width of `pass` (the last pass may take fewer bits).
+__device__ __forceinline__ uint32_t pass_buckets(const PlanArgs& a, int pass) {
+  return 1u << min(a.digit_bits, a.id_bits - pass * a.digit_bits);
+}
+
+__global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
   __shared__ long long sw64[kTileThreads / 32];
   const int t = threadIdx.x, tile = blockIdx.x;
-  const int B = a.passes ? 1 << min(a.digit_bits, a.id_bits) : 0;
-  for (int i = t; i < B; i += kTileThreads) h[i] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
-  __syncthreads();
   int bad = 0;
   long long raw[kTileItems];
 #pragma unroll
@@ -556,115 +644,90 @@ __global__ void __launch_bounds__(kTileThreads) pack_hist_kernel(PlanArgs a) {
     }
     a.keys_a[i] = k;
     a.vals_a[i] = static_cast<uint32_t>(i);
-    if (B) atomicAdd(&h[k & (B - 1)], 1u);
   }
   bad = static_cast<int>(block_sum<kTileThreads>(bad, sw64));
-  __syncthreads();
-  for (int d = t; d < B; d += kTileThreads) a.hist[static_cast<long long>(d) * a.tiles + tile] = h[d];
   if (t == 0) a.tile_bad[tile] = bad;
+  // clear this tile's look-back words, and (tile 0) the digit totals, the tile counters
+  // and the status word, which later kernels may set to an error
+  constexpr int B = 1 << kMaxDigitBits;
+  for (int p = 0; p < a.passes; ++p)
+    for (int d = t; d < B; d += kTileThreads) a.sweep[(static_cast<long long>(p) * a.tiles + tile) * B + d] = 0;
+  if (t < 4) a.list_status[tile * 4 + t] = 0;
+  if (tile == 0) {
+    for (int i = t; i < kMaxPasses * B; i += kTileThreads) a.totals[i] = 0;
+    if (t <= kMaxPasses) a.counters[t] = 0;
+    if (t == 0) a.header->status = EWG_OK;
+  }
 }
 
-// Digit histogram of each tile for pass >= 1.
-__global__ void __launch_bounds__(kTileThreads) hist_kernel(PlanArgs a, const uint32_t* keys,
-                                                            int pass) {
-  __shared__ uint32_t h[1 << kMaxDigitBits];
+// Keys per digit of every pass, over all tiles.
+__global__ void __launch_bounds__(kTileThreads) hist_kernel(PlanArgs a) {
+  constexpr int B = 1 << kMaxDigitBits;
+  __shared__ uint32_t h[kMaxPasses * B];
   const int t = threadIdx.x, tile = blockIdx.x;
-  const int sh = pass * a.digit_bits;
-  const int B = 1 << min(a.digit_bits, a.id_bits - sh);
-  for (int i = t; i < B; i += kTileThreads) h[i] = 0;
+  for (int i = t; i < kMaxPasses * B; i += kTileThreads) h[i] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
   __syncthreads();
-  for (int r = 0; r < kTileItems; ++r) {
-    const uint32_t k = keys[tile * kTile + r * kTileThreads + t];
-    atomicAdd(&h[(k >> sh) & (B - 1)], 1u);
+  // one atomic per distinct digit per warp: a hot id would otherwise serialise a warp
+  // on one counter
+  const int lane = t & 31;
+  uint32_t key[kTileItems];
+#pragma unroll
+  for (int r = 0; r < kTileItems; ++r) key[r] = a.keys_a[tile * kTile + r * kTileThreads + t];
+  for (int p = 0; p < a.passes; ++p) {
+    const uint32_t mask = pass_buckets(a, p) - 1u;
+#pragma unroll
+    for (int r = 0; r < kTileItems; ++r) {
+      const uint32_t d = (key[r] >> (p * a.digit_bits)) & mask;
+      const unsigned peers = __match_any_sync(kFull, d);
+      if (lane == __ffs(peers) - 1) atomicAdd(&h[p * B + d], static_cast<uint32_t>(__popc(peers)));
+    }
   }
   __syncthreads();
-  for (int d = t; d < B; d += kTileThreads) a.hist[static_cast<long long>(d) * a.tiles + tile] = h[d];
+  for (int i = t; i < a.passes * B; i += kTileThreads)
+    if (h[i]) atomicAdd(&a.totals[i], h[i]);
 }
 
-// Exclusive scan of hist[bucket][tile] in (bucket, tile) order: each (bucket, tile)
-// gets the first output slot of its keys.  Rounds of 16 entries per thread: each thread
-// loads its 16 consecutive entries at once, the block scans the per-thread sums, and a
-// carry links the rounds.
-__global__ void __launch_bounds__(1024) scan_hist_kernel(PlanArgs a, int pass) {
-  constexpr int IT = 16;
-  __shared__ long long sw64[32];
-  ptx::pdl_wait_prior_grid();
-  ptx::pdl_launch_dependents();
-  const int t = threadIdx.x;
-  const int sh = pass * a.digit_bits;
-  const long long E = static_cast<long long>(1 << min(a.digit_bits, a.id_bits - sh)) * a.tiles;
-  long long carry = 0;
-  for (long long base = 0; base < E; base += 1024 * IT) {
-    const long long i0 = base + static_cast<long long>(t) * IT;
-    uint32_t v[IT];
-    if (i0 + IT <= E) {   // 64-byte aligned: the region is 256-byte aligned, i0 % 16 == 0
-      const uint4* src = reinterpret_cast<const uint4*>(a.hist + i0);
-#pragma unroll
-      for (int q = 0; q < IT / 4; ++q) {
-        const uint4 x = src[q];
-        v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < IT; ++k) v[k] = i0 + k < E ? a.hist[i0 + k] : 0u;
-    }
-    long long local = 0;
-#pragma unroll
-    for (int k = 0; k < IT; ++k) local += v[k];
-    long long round_total = 0;
-    long long run = carry + block_exclusive_scan<1024, long long>(local, SumOp(), 0ll, sw64,
-                                                                  &round_total);
-#pragma unroll
-    for (int k = 0; k < IT; ++k) {
-      const uint32_t c = v[k];
-      v[k] = static_cast<uint32_t>(run);
-      run += c;
-    }
-    if (i0 + IT <= E) {
-      uint4* dst = reinterpret_cast<uint4*>(a.hist + i0);
-#pragma unroll
-      for (int q = 0; q < IT / 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-    } else {
-#pragma unroll
-      for (int k = 0; k < IT; ++k)
-        if (i0 + k < E) a.hist[i0 + k] = v[k];
-    }
-    carry += round_total;
-  }
-}
-
-// Stable scatter of one tile for one pass.  Every global load of the tile (keys,
-// positions, the tile's output bases of this thread's digits) is issued up front.
-__global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const uint32_t* ks,
-                                                               const uint32_t* vs, uint32_t* kd,
-                                                               uint32_t* vd, int pass) {
+// One stable LSD radix pass: (ks, vs) -> (kd, vd), ordered by the digit of `pass`.
+__global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const uint32_t* ks,
+                                                             const uint32_t* vs, uint32_t* kd,
+                                                             uint32_t* vd, int pass) {
   constexpr int NW = kTileThreads / 32;
   constexpr int kStride = 1 << kMaxDigitBits;
-  constexpr int kDigitsPerThread = kStride / kTileThreads;
-  __shared__ uint32_t cnt[NW * kStride];   // [warp][bucket]
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, tile = blockIdx.x;
+  constexpr int kDpt = kStride / kTileThreads;   // digits per thread, consecutive
+  __shared__ uint32_t cnt[NW * kStride];          // [warp][digit]
+  __shared__ uint32_t base[kStride];              // first output slot of the tile's digit
+  __shared__ uint32_t sw[NW];
+  __shared__ int s_tile, s_ok;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int sh = pass * a.digit_bits;
-  const uint32_t B = 1u << min(a.digit_bits, a.id_bits - sh), mask = B - 1;
+  const uint32_t B = pass_buckets(a, pass), mask = B - 1;
   const uint32_t lt = (1u << lane) - 1u;
   for (int w = 0; w < NW; ++w)
     for (uint32_t d = t; d < B; d += kTileThreads) cnt[w * kStride + d] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
-  uint32_t key[kTileItems], val[kTileItems], hb[kDigitsPerThread];
+  if (t == 0) {
+    s_ok = a.header->status == EWG_OK;
+    s_tile = atomicAdd(&a.counters[pass], 1);
+  }
+  uint32_t tot[kDpt];
+#pragma unroll
+  for (int j = 0; j < kDpt; ++j) {
+    const uint32_t d = t * kDpt + j;
+    tot[j] = d < B ? a.totals[pass * kStride + d] : 0u;
+  }
+  __syncthreads();
+  if (!s_ok) return;
+  const int tile = s_tile;
+  uint32_t key[kTileItems], val[kTileItems];
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
     const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
     key[r] = ks[idx];
     val[r] = vs[idx];
   }
-#pragma unroll
-  for (int j = 0; j < kDigitsPerThread; ++j) {
-    const uint32_t d = t + j * kTileThreads;
-    hb[j] = d < B ? a.hist[static_cast<long long>(d) * a.tiles + tile] : 0u;
-  }
-  __syncthreads();
   uint32_t rank[kTileItems], dig[kTileItems];
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
@@ -678,22 +741,59 @@ __global__ void __launch_bounds__(kTileThreads) scatter_kernel(PlanArgs a, const
     dig[r] = d;
   }
   __syncthreads();
+  // the tile's count of each digit; cnt becomes the per-warp offsets within the tile
+  uint32_t own[kDpt];
 #pragma unroll
-  for (int j = 0; j < kDigitsPerThread; ++j) {
-    const uint32_t d = t + j * kTileThreads;
-    if (d < B) {
-      uint32_t run = hb[j];
+  for (int j = 0; j < kDpt; ++j) {
+    const uint32_t d = t * kDpt + j;
+    uint32_t run = 0;
+    if (d < B)
       for (int w = 0; w < NW; ++w) {
         const uint32_t c = cnt[w * kStride + d];
         cnt[w * kStride + d] = run;
         run += c;
       }
-    }
+    own[j] = run;
   }
-  __syncthreads();
+  uint32_t* words = a.sweep + static_cast<long long>(pass) * a.tiles * kStride;
+#pragma unroll
+  for (int j = 0; j < kDpt; ++j) {
+    const uint32_t d = t * kDpt + j;
+    if (d < B) st_relaxed(words + static_cast<long long>(tile) * kStride + d, (tile ? kFlagAgg : kFlagInc) | own[j]);
+  }
+  // digits before d over all keys (totals), plus digit d in the tiles before this one
+  uint32_t sum = 0;
+#pragma unroll
+  for (int j = 0; j < kDpt; ++j) sum += tot[j];
+  uint32_t below = static_cast<uint32_t>(
+      block_exclusive_scan<kTileThreads, int>(static_cast<int>(sum), SumIntOp(), 0, reinterpret_cast<int*>(sw), nullptr));
+  bool ok = true;
+  uint32_t before[kDpt];
+  {
+    uint32_t* w[kDpt];
+    bool act[kDpt];
+#pragma unroll
+    for (int j = 0; j < kDpt; ++j) {
+      w[j] = words + t * kDpt + j;
+      act[j] = t * kDpt + j < B;
+      before[j] = 0;
+    }
+    if (tile > 0) ok = look_back<16, kDpt>(w, kStride, tile, act, own, before);
+  }
+#pragma unroll
+  for (int j = 0; j < kDpt; ++j) {
+    const uint32_t d = t * kDpt + j;
+    if (d < B) base[d] = below + before[j];
+    below += tot[j];
+  }
+  if (__syncthreads_or(!ok)) {
+    if (t == 0) give_up_plan(a);
+    return;
+  }
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
-    const uint32_t dst = cnt[warp * kStride + dig[r]] + rank[r];
+    const uint32_t dst = base[dig[r]] + cnt[warp * kStride + dig[r]] + rank[r];
+    if (!checked(dst < static_cast<uint32_t>(a.tiles) * kTile, a.header)) continue;
     kd[dst] = key[r];
     vd[dst] = val[r];
   }
@@ -741,83 +841,67 @@ __device__ void tile_seeds(const uint32_t* keys, int n, int s0, int* rs_seed, in
   *re_seed = seeds[1];
 }
 
-__global__ void __launch_bounds__(kTileThreads) list_count_kernel(PlanArgs a,
-                                                                  const uint32_t* keys) {
+// Runs and chunks of the sorted keys, one tile per CTA (tiles in claim order).
+__global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const uint32_t* keys,
+                                                            const uint32_t* vals) {
   __shared__ int swi[kTileThreads / 32];
   __shared__ long long sw64[kTileThreads / 32];
+  __shared__ int s_tile, s_ok;
+  __shared__ uint32_t s_before[3], s_own[3];
+  const int t = threadIdx.x;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
-  const int s0 = blockIdx.x * kTile;
+  if (t == 0) {
+    s_ok = a.header->status == EWG_OK;
+    s_tile = atomicAdd(&a.counters[kMaxPasses], 1);
+  }
+  long long bad = 0;
+  for (int i = t; i < a.tiles; i += kTileThreads) bad += a.tile_bad[i];
+  bad = block_sum<kTileThreads>(bad, sw64);   // its barriers also publish s_ok and s_tile
+  if (!s_ok) return;
+  const int tile = s_tile;
+  if (bad) {   // nothing is listed; the first tile reports the bad ids
+    if (tile == 0 && t == 0) {
+      write_header_fields(a, 1, static_cast<int>(bad));
+      atomicExch(&a.header->status, EWG_ERR_ID_OUT_OF_RANGE);
+    }
+    return;
+  }
+  const int s0 = tile * kTile;
   int rs_seed, re_seed;
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
-  if (threadIdx.x == 0) {   // the sort is done with the histograms: keep the seeds there
-    a.hist[2 * blockIdx.x] = static_cast<uint32_t>(rs_seed);
-    a.hist[2 * blockIdx.x + 1] = static_cast<uint32_t>(re_seed);
-  }
   Listing<kTileThreads, kTileItems> L;
   L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
-  const long long tot = block_sum<kTileThreads>(L.counts(a.n, s0, a.skip_key), sw64);
-  if (threadIdx.x == 0)
-    a.tile_cnt[blockIdx.x] = make_int4(field_long(tot), field_short(tot), field_runs(tot), 0);
-}
-
-// Scans the per-tile counts, sums the bad-id counts, writes the header and the
-// (single-partition) tables.
-__global__ void __launch_bounds__(1024) list_scan_kernel(PlanArgs a) {
-  __shared__ long long sw64[32];
-  ptx::pdl_wait_prior_grid();
-  ptx::pdl_launch_dependents();
-  const int t = threadIdx.x;
-  const int per = (a.tiles + 1023) / 1024;
-  const int b0 = min(a.tiles, t * per), b1 = min(a.tiles, b0 + per);
-  long long l = 0, s = 0, r = 0, bad = 0;
-  for (int i = b0; i < b1; ++i) {
-    const int4 c = a.tile_cnt[i];
-    l += c.x;
-    s += c.y;
-    r += c.z;
-    bad += a.tile_bad[i];
+  long long tot = 0;
+  const long long prefix = block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0, a.skip_key),
+                                                                         SumOp(), 0ll, sw64, &tot);
+  if (t < 3) {   // one look-back chain each: long chunks, short chunks, long-run entries
+    const uint32_t own = static_cast<uint32_t>(t == 0 ? field_long(tot) : t == 1 ? field_short(tot) : field_runs(tot));
+    uint32_t* word[1] = {a.list_status + t};
+    st_relaxed(word[0] + tile * 4, (tile ? kFlagAgg : kFlagInc) | own);
+    const bool act[1] = {true};
+    const uint32_t mine[1] = {own};
+    uint32_t before[1] = {0};
+    const bool ok = tile == 0 || look_back<32, 1>(word, 4, tile, act, mine, before);
+    s_before[t] = ok ? before[0] : 0xffffffffu;
+    s_own[t] = own;
   }
-  long long tl = 0, ts = 0, tr = 0;
-  long long pl = block_exclusive_scan<1024, long long>(l, SumOp(), 0ll, sw64, &tl);
-  long long ps = block_exclusive_scan<1024, long long>(s, SumOp(), 0ll, sw64, &ts);
-  long long pr = block_exclusive_scan<1024, long long>(r, SumOp(), 0ll, sw64, &tr);
-  for (int i = b0; i < b1; ++i) {
-    const int4 c = a.tile_cnt[i];
-    a.tile_cnt[i] = make_int4(static_cast<int>(pl), static_cast<int>(ps), static_cast<int>(pr), 0);
-    pl += c.x;
-    ps += c.y;
-    pr += c.z;
+  __syncthreads();
+  if (s_before[0] == 0xffffffffu || s_before[1] == 0xffffffffu || s_before[2] == 0xffffffffu) {
+    if (t == 0) give_up_plan(a);
+    return;
   }
-  const long long bad_total = block_sum<1024>(bad, sw64);
-  if (t == 0) {
-    write_tables(a, 0, static_cast<int>(tl), 0, static_cast<int>(ts), static_cast<int>(tl),
-                 static_cast<int>(tr), 0);
-    write_header(a, 1, static_cast<int>(bad_total));
-  }
-}
-
-__global__ void __launch_bounds__(kTileThreads) list_emit_kernel(PlanArgs a, const uint32_t* keys,
-                                                                 const uint32_t* vals) {
-  __shared__ int swi[kTileThreads / 32];
-  __shared__ long long sw64[kTileThreads / 32];
-  ptx::pdl_wait_prior_grid();
-  ptx::pdl_launch_dependents();
-  if (a.header->status != EWG_OK) return;
-  const int s0 = blockIdx.x * kTile;
-  const int rs_seed = static_cast<int>(a.hist[2 * blockIdx.x]);
-  const int re_seed = static_cast<int>(a.hist[2 * blockIdx.x + 1]);
-  Listing<kTileThreads, kTileItems> L;
-  L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
-  const long long prefix =
-      block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0, a.skip_key), SumOp(), 0ll, sw64, nullptr);
-  const int4 tp = a.tile_cnt[blockIdx.x];
   EmitBases eb;
-  eb.long_desc = tp.x;
-  eb.short_desc = a.tables[kLongCnt * kMaxParts] + tp.y;
-  eb.partial = tp.x;
-  eb.run = tp.z;
+  eb.long_desc = static_cast<int>(s_before[0]);
+  eb.short_desc = a.short_base + static_cast<int>(s_before[1]);
+  eb.partial = static_cast<int>(s_before[0]);
+  eb.run = static_cast<int>(s_before[2]);
   L.emit(a, vals, a.n, s0, prefix, eb);
+  if (tile == a.tiles - 1 && t == 0) {
+    write_tables(a, 0, static_cast<int>(s_before[0] + s_own[0]), 0, static_cast<int>(s_before[1] + s_own[1]),
+                 a.short_base, static_cast<int>(s_before[2] + s_own[2]), 0);
+    write_header_fields(a, 1, 0);
+  }
 }
 
 }  // namespace
@@ -854,15 +938,14 @@ cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   if (a.n <= kHashMaxN) return launch_pdl(plan_hashed_kernel, kHashParts, kHashThreads, kHashSmem, stream, a);
   const int tiles = a.tiles;
-  cudaError_t e = launch_pdl(pack_hist_kernel, tiles, kTileThreads, 0, stream, a);
+  cudaError_t e = launch_pdl(pack_kernel, tiles, kTileThreads, 0, stream, a);
+  if (e == cudaSuccess && a.passes > 0) e = launch_pdl(hist_kernel, tiles, kTileThreads, 0, stream, a);
   const uint32_t* ks = a.keys_a;
   const uint32_t* vs = a.vals_a;
   uint32_t* kd = a.keys_b;
   uint32_t* vd = a.vals_b;
   for (int pass = 0; pass < a.passes && e == cudaSuccess; ++pass) {
-    if (pass > 0) e = launch_pdl(hist_kernel, tiles, kTileThreads, 0, stream, a, ks, pass);
-    if (e == cudaSuccess) e = launch_pdl(scan_hist_kernel, 1, 1024, 0, stream, a, pass);
-    if (e == cudaSuccess) e = launch_pdl(scatter_kernel, tiles, kTileThreads, 0, stream, a, ks, vs, kd, vd, pass);
+    e = launch_pdl(sweep_kernel, tiles, kTileThreads, 0, stream, a, ks, vs, kd, vd, pass);
     const uint32_t* nk = kd;
     const uint32_t* nv = vd;
     kd = const_cast<uint32_t*>(ks);
@@ -870,9 +953,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
     ks = nk;
     vs = nv;
   }
-  if (e == cudaSuccess) e = launch_pdl(list_count_kernel, tiles, kTileThreads, 0, stream, a, ks);
-  if (e == cudaSuccess) e = launch_pdl(list_scan_kernel, 1, 1024, 0, stream, a);
-  if (e == cudaSuccess) e = launch_pdl(list_emit_kernel, tiles, kTileThreads, 0, stream, a, ks, vs);
+  if (e == cudaSuccess) e = launch_pdl(list_kernel, tiles, kTileThreads, 0, stream, a, ks, vs);
   return e;
 }
 

@@ -68,6 +68,10 @@ extern "C" {
 #define EWG_ERR_ID_OUT_OF_RANGE 4 /* device-detected: an id outside [0, num_embeddings) */
 #define EWG_ERR_TIMEOUT 5         /* device-detected: a bounded wait in a kernel gave up;
                                      touched main_grad rows are then unspecified */
+#define EWG_ERR_BOUNDS 6          /* device-detected, bounds-checking build (libewg_debug.so)
+                                     only: an index a kernel derived from the plan was out of
+                                     range; the access was replaced by a safe one, so
+                                     main_grad's touched rows are then unspecified */
 
 /*
  * Whether ewg_accumulate supports these tensors (can_accumulate_embedding_wgrad on

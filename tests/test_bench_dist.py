@@ -65,6 +65,8 @@ def test_launch_count_claim():
 
     # hashed plan (one kernel) + the apply kernel
     assert bench.kernel_launches_per_call(8192, 129280) == 2
-    # 17 id bits -> two 9-bit passes: pack, 2 x (scan, scatter), 1 histogram, 3 listing
-    # kernels, plus the apply kernel
-    assert bench.kernel_launches_per_call(65536, 129280) == 1 + 4 + 1 + 3 + 1
+    # 17 id bits -> two 9-bit passes: pack, the digit histogram, one sweep per pass, the
+    # listing, plus the apply kernel
+    assert bench.kernel_launches_per_call(65536, 129280) == 1 + 1 + 2 + 1 + 1
+    # a one-row table needs no radix pass: pack, listing, apply
+    assert bench.kernel_launches_per_call(65536, 1) == 1 + 1 + 1

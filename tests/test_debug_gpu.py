@@ -1,0 +1,82 @@
+"""The bounds-checking build (libewg_debug.so): the same kernels with every index they
+derive from the plan checked.  It must give the oracle's bits on ordinary inputs, and
+when a plan entry is corrupted from the host it must report EWG_ERR_BOUNDS through the
+status word and finish without touching memory outside its buffers.  The corruption is
+only ever applied to the checked build."""
+import ctypes
+
+import pytest
+import torch
+
+import embedding_weight_grad_gb300 as ewg
+import workloads
+from test_parity_gpu import DEV, assert_same_bits, oracle_expected
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dlib():
+    from embedding_weight_grad_gb300 import build
+    build.build(debug=True)
+    return ewg.debug_lib()
+
+
+def stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def status_of(L, ws):
+    st = ctypes.c_int(-1)
+    assert L.ewg_read_status(ws.data_ptr(), stream(), ctypes.byref(st)) == ewg.OK
+    return st.value
+
+
+def inputs(name, hidden):
+    w = workloads.BY_NAME[name]
+    if hidden:
+        w = workloads.scaled(w, hidden=hidden)
+    ids_np = workloads.make_ids(w)
+    ids = torch.from_numpy(ids_np.reshape(-1)).to(DEV)
+    grad = workloads.make_grad(w, DEV).reshape(ids.numel(), w.hidden)
+    mg = workloads.make_main_grad(w, DEV)
+    return ids_np, ids, grad, mg
+
+
+@pytest.mark.parametrize("name,hidden", [("tiny", None), ("long_runs", 264)])
+def test_debug_build_matches_oracle(oracle_mod, dlib, name, hidden):
+    ids_np, ids, grad, mg = inputs(name, hidden)
+    before = mg.clone()
+    ws = ewg.new_workspace(ids.numel(), mg.shape[1], DEV)
+    a = ewg._Args(ids, grad, mg)
+    assert dlib.ewg_accumulate(*a.c_args(), ws.data_ptr(), ws.numel(), stream()) == ewg.OK
+    assert status_of(dlib, ws) == ewg.OK
+    torch.cuda.synchronize()
+    assert_same_bits(mg, oracle_expected(oracle_mod, ids_np, grad, before))
+
+
+@pytest.mark.parametrize("name,hidden", [("gpt2_like", None), ("long_runs", 264)])
+def test_debug_build_reports_a_corrupted_plan(dlib, name, hidden):
+    """Descriptor 0 (a chunk of the plan, on either plan path) gets a position beyond the
+    last token between ewg_plan and ewg_apply."""
+    _, ids, grad, mg = inputs(name, hidden)
+    n, H, V = ids.numel(), mg.shape[1], mg.shape[0]
+    ws = ewg.new_workspace(n, H, DEV)
+    assert dlib.ewg_plan(ids.data_ptr(), 1, n, V, H, ws.data_ptr(), ws.numel(), stream()) == ewg.OK
+    assert status_of(dlib, ws) == ewg.OK
+    chunks_at = chunk_region_offset(dlib, n, H)
+    ws[chunks_at:chunks_at + 4].view(torch.int32).fill_(n + 12345)   # position word 0
+    assert dlib.ewg_apply(grad.data_ptr(), ewg._BF16, H, mg.data_ptr(), ewg._FP32 if mg.dtype == torch.float32
+                          else ewg._BF16, n, V, H, H, ws.data_ptr(), ws.numel(), stream()) == ewg.OK
+    assert status_of(dlib, ws) == ewg.ERR_BOUNDS
+
+
+def chunk_region_offset(L, n, H):
+    """Byte offset of the chunk descriptors in the workspace: after the 256-byte header,
+    the partition tables (6 x 128 ints) and four key / position arrays of ceil(n / 2048) *
+    2048 words each (internal layout, every region 256-byte aligned)."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    n_pad = -(-n // 2048) * 2048
+    off = up(256) + up(6 * 128 * 4)
+    return off + 4 * up(n_pad * 4)
