@@ -199,9 +199,8 @@ int do_plan(const void* ids, int ids_dtype, int64_t n, int64_t V, int64_t row_be
   a.partial_cap = static_cast<int>(ewg::max_partial_rows(n));
   a.short_base = static_cast<int>(L.short_base);
   a.runs = at<int>(ws, L.runs);
-  a.sweep = at<uint32_t>(ws, L.sweep);
-  a.totals = at<uint32_t>(ws, L.ctl);
-  a.counters = a.totals + ewg::kMaxPasses * (1 << ewg::kMaxDigitBits);
+  a.tile_hist = at<uint32_t>(ws, L.tile_hist);
+  a.counters = at<uint32_t>(ws, L.ctl);
   a.tile_bad = at<int>(ws, L.tile_bad);
   a.list_status = at<uint32_t>(ws, L.list_status);
   a.arrivals = at<int>(ws, L.arrivals);

@@ -156,7 +156,7 @@ inline int64_t max_partial_rows(int64_t n) { return 2 * n / 11 + kMaxParts + 1; 
 inline int64_t max_long_runs(int64_t n) { return n / 11 + n / 100 + kMaxParts + 1; }
 
 struct Layout {
-  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, sweep, ctl, tile_bad, list_status,
+  size_t header, tables, keys_a, vals_a, keys_b, vals_b, chunks, runs, tile_hist, ctl, tile_bad, list_status,
       arrivals, partial, total;
   int64_t n, hidden, tiles;
   int64_t short_base;   // multi-tile plan: descriptor index of the first short chunk
@@ -185,8 +185,8 @@ inline Layout make_layout(int64_t n, int64_t hidden) {
   L.short_base = max_partial_rows(n);
   L.chunks = take(static_cast<size_t>(L.short_base + n) * kChunkWords * 4);
   L.runs = take(static_cast<size_t>(max_long_runs(n)) * kRunWords * 4);
-  L.sweep = take(static_cast<size_t>(kMaxPasses) * L.tiles * (1 << kMaxDigitBits) * 4);
-  L.ctl = take(static_cast<size_t>(kMaxPasses * (1 << kMaxDigitBits) + kMaxPasses + 1) * 4);
+  L.tile_hist = take(static_cast<size_t>(kMaxPasses) * L.tiles * (1 << kMaxDigitBits) * 4);
+  L.ctl = take(static_cast<size_t>(kMaxPasses + 1) * 4);
   L.tile_bad = take(static_cast<size_t>(L.tiles) * 4);
   L.list_status = take(static_cast<size_t>(L.tiles) * 16);
   L.arrivals = take(static_cast<size_t>(max_partial_rows(n)) * 4);
@@ -244,9 +244,8 @@ struct PlanArgs {
   int partial_cap;
   int short_base;        // multi-tile plan: descriptor index of the first short chunk
   int* runs;
-  uint32_t* sweep;       // [pass][tile][bucket] look-back words of the radix sweeps
-  uint32_t* totals;      // [pass][bucket] keys per digit over all tiles
-  uint32_t* counters;    // [pass] tiles claimed by each sweep, [kMaxPasses] by the listing
+  uint32_t* tile_hist;   // [pass][tile][digit]: keys of each digit in each tile of the pass
+  uint32_t* counters;    // [kMaxPasses]: tiles claimed by the listing
   int* tile_bad;         // per tile: ids outside [0, num_embeddings)
   uint32_t* list_status; // per tile, 4 words: look-back words of long chunks, short chunks, long runs
   int* arrivals;         // per long run, at its first partial row: zeroed here

@@ -541,18 +541,25 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
 // ---------------------------------------------------------------------------
 // Multi-tile plan: tiles of kTile keys, one CTA each.
 //
-//   pack    each tile's keys (the id, or a skip / pad key) and positions; counts its bad
-//           ids; clears what the later kernels count into
-//   hist    digit histograms of every radix pass over all keys (global atomics)
-//   sweep   one per radix pass: a stable scatter in which each tile ranks its keys by
-//           digit, publishes its digit counts and sums the counts of the tiles before it
-//           by decoupled look-back.  Tiles are taken in claim order from a counter, so
-//           the tiles before a running one are running or done and every wait ends.
+//   pack    each tile's keys (the id, or a skip / pad key) and positions, its bad ids and
+//           its digit histogram for the first radix pass; clears what later kernels count
+//           into
+//   sweep   one per radix pass: a stable scatter.  Each tile sums the histogram columns
+//           of its digits over all tiles (keys of smaller digits come first) and over the
+//           tiles before it (its own keys of a digit follow theirs), ranks its keys and
+//           scatters them; it also counts, per destination tile, the digits of the next
+//           pass, so the next sweep finds its histograms complete.  No tile waits for
+//           another.
 //   list    runs and chunks of the sorted keys: each tile counts its chunks and runs,
-//           sums the counts of the tiles before it by the same look-back, and writes its
-//           descriptors; the last tile writes the tables and the header.
-// Every look-back poll is bounded; a tile that gives up sets EWG_ERR_TIMEOUT and the
-// kernels after it write nothing.
+//           sums the counts of the tiles before it by decoupled look-back (tiles are taken
+//           in claim order, so the tiles before a running one are running or done, and
+//           every poll is bounded), and writes its descriptors; the last tile writes the
+//           tables and the header.
+// A look-back that gives up sets EWG_ERR_TIMEOUT and the tile writes nothing.
+//
+// Each sweep reads the histograms of all tiles for its digits: tiles x 2 KB per CTA, one
+// round of loads up to a few hundred tiles, growing with the square of the tile count
+// beyond.
 
 constexpr uint32_t kFlagAgg = 1u << 30;   // the word holds the tile's own count
 constexpr uint32_t kFlagInc = 2u << 30;   // ... the sum over the tile and all before it
@@ -572,10 +579,11 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 // Look-back over NCH chains of words at once (chain c: tile j's word at word[c] + j *
 // stride).  This tile has published its own counts as aggregates (or, as tile 0, as
 // inclusive sums).  Each round loads the words of the K closest predecessors not yet
-// summed, all in flight together, then adds them from the closest one on until a word
-// holds an inclusive sum; since every tile publishes its aggregate early, a round
-// usually settles a chain of up to K tiles in one round trip.  Publishes this tile's
-// inclusive sums.  False if a predecessor published nothing within the poll limit.
+// summed, all in flight together, and polls again, together, those not yet published
+// before the first inclusive one; it then adds them from the closest on until a word holds
+// an inclusive sum.  Every tile publishes its aggregate early, so a round usually settles
+// up to K tiles in one or two round trips.  Publishes this tile's inclusive sums.  False if
+// a predecessor published nothing within the poll limit.
 template <int K, int NCH>
 __device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int tile, const bool (&active)[NCH],
                           const uint32_t (&own)[NCH], uint32_t (&excl)[NCH]) {
@@ -588,17 +596,29 @@ __device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int ti
       uint32_t v[K];
 #pragma unroll
       for (int i = 0; i < K; ++i) v[i] = i < m ? ld_relaxed(word[c] + (hi - 1 - i) * stride) : kFlagInc;
+      for (int poll = 0;; ++poll) {
+        bool pending = false, inc = false;   // an unpublished word before the first inclusive
+#pragma unroll
+        for (int i = 0; i < K; ++i) {
+          if (i < m && !inc && !pending) {
+            pending = !(v[i] & ~kCountMask);
+            inc = (v[i] & kFlagInc) != 0;
+          }
+        }
+        if (!pending) break;
+        if (poll >= kLookBackPolls) return false;
+        __nanosleep(32);
+#pragma unroll
+        for (int i = 0; i < K; ++i)
+          if (i < m && !(v[i] & ~kCountMask)) v[i] = ld_relaxed(word[c] + (hi - 1 - i) * stride);
+      }
       bool stop = false;
 #pragma unroll
       for (int i = 0; i < K; ++i) {
-        if (i >= m || stop) continue;
-        for (int p = 0; p < kLookBackPolls && !(v[i] & ~kCountMask); ++p) {
-          __nanosleep(32);
-          v[i] = ld_relaxed(word[c] + (hi - 1 - i) * stride);
+        if (i < m && !stop) {
+          sum += v[i] & kCountMask;
+          stop = (v[i] & kFlagInc) != 0;
         }
-        if (!(v[i] & ~kCountMask)) return false;
-        sum += v[i] & kCountMask;
-        stop = (v[i] & kFlagInc) != 0;
       }
       if (stop) break;
       hi -= m;
@@ -617,8 +637,11 @@ __device__ __forceinline__ uint32_t pass_buckets(const PlanArgs& a, int pass) {
 }
 
 __global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
+  constexpr int B = 1 << kMaxDigitBits;
   __shared__ long long sw64[kTileThreads / 32];
-  const int t = threadIdx.x, tile = blockIdx.x;
+  __shared__ uint32_t h[B];
+  const int t = threadIdx.x, lane = t & 31, tile = blockIdx.x;
+  for (int d = t; d < B; d += kTileThreads) h[d] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
   int bad = 0;
@@ -628,6 +651,8 @@ __global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
     const int i = tile * kTile + r * kTileThreads + t;
     raw[r] = i < a.n ? load_id(a.ids, a.ids_int64, i) : 0;
   }
+  __syncthreads();   // h is clear
+  const uint32_t mask0 = a.passes ? pass_buckets(a, 0) - 1u : 0u;
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
     const int i = tile * kTile + r * kTileThreads + t;
@@ -644,49 +669,26 @@ __global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
     }
     a.keys_a[i] = k;
     a.vals_a[i] = static_cast<uint32_t>(i);
+    if (a.passes) {   // one atomic per distinct digit per warp: a hot id would serialise
+      const uint32_t d = k & mask0;
+      const unsigned peers = __match_any_sync(kFull, d);
+      if (lane == __ffs(peers) - 1) atomicAdd(&h[d], static_cast<uint32_t>(__popc(peers)));
+    }
   }
-  bad = static_cast<int>(block_sum<kTileThreads>(bad, sw64));
+  bad = static_cast<int>(block_sum<kTileThreads>(bad, sw64));   // its barriers also complete h
   if (t == 0) a.tile_bad[tile] = bad;
-  // clear this tile's look-back words, and (tile 0) the digit totals, the tile counters
-  // and the status word, which later kernels may set to an error
-  constexpr int B = 1 << kMaxDigitBits;
-  for (int p = 0; p < a.passes; ++p)
-    for (int d = t; d < B; d += kTileThreads) a.sweep[(static_cast<long long>(p) * a.tiles + tile) * B + d] = 0;
+  // this tile's histogram of the first pass; its rows of the later passes start at zero
+  // (the sweep before each of them counts into them)
+  for (int p = 0; p < a.passes; ++p) {
+    const int Bp = static_cast<int>(pass_buckets(a, p));
+    uint32_t* row = a.tile_hist + (static_cast<long long>(p) * a.tiles + tile) * B;
+    for (int d = t; d < Bp; d += kTileThreads) row[d] = p == 0 ? h[d] : 0u;
+  }
   if (t < 4) a.list_status[tile * 4 + t] = 0;
   if (tile == 0) {
-    for (int i = t; i < kMaxPasses * B; i += kTileThreads) a.totals[i] = 0;
     if (t <= kMaxPasses) a.counters[t] = 0;
     if (t == 0) a.header->status = EWG_OK;
   }
-}
-
-// Keys per digit of every pass, over all tiles.
-__global__ void __launch_bounds__(kTileThreads) hist_kernel(PlanArgs a) {
-  constexpr int B = 1 << kMaxDigitBits;
-  __shared__ uint32_t h[kMaxPasses * B];
-  const int t = threadIdx.x, tile = blockIdx.x;
-  for (int i = t; i < kMaxPasses * B; i += kTileThreads) h[i] = 0;
-  ptx::pdl_wait_prior_grid();
-  ptx::pdl_launch_dependents();
-  __syncthreads();
-  // one atomic per distinct digit per warp: a hot id would otherwise serialise a warp
-  // on one counter
-  const int lane = t & 31;
-  uint32_t key[kTileItems];
-#pragma unroll
-  for (int r = 0; r < kTileItems; ++r) key[r] = a.keys_a[tile * kTile + r * kTileThreads + t];
-  for (int p = 0; p < a.passes; ++p) {
-    const uint32_t mask = pass_buckets(a, p) - 1u;
-#pragma unroll
-    for (int r = 0; r < kTileItems; ++r) {
-      const uint32_t d = (key[r] >> (p * a.digit_bits)) & mask;
-      const unsigned peers = __match_any_sync(kFull, d);
-      if (lane == __ffs(peers) - 1) atomicAdd(&h[p * B + d], static_cast<uint32_t>(__popc(peers)));
-    }
-  }
-  __syncthreads();
-  for (int i = t; i < a.passes * B; i += kTileThreads)
-    if (h[i]) atomicAdd(&a.totals[i], h[i]);
 }
 
 // One stable LSD radix pass: (ks, vs) -> (kd, vd), ordered by the digit of `pass`.
@@ -695,12 +697,13 @@ __global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const u
                                                              uint32_t* vd, int pass) {
   constexpr int NW = kTileThreads / 32;
   constexpr int kStride = 1 << kMaxDigitBits;
-  constexpr int kDpt = kStride / kTileThreads;   // digits per thread, consecutive
+  constexpr int kBatch = 32;                      // histogram rows loaded together
+  static_assert(kStride == 2 * kTileThreads, "each thread owns two consecutive digits");
   __shared__ uint32_t cnt[NW * kStride];          // [warp][digit]
   __shared__ uint32_t base[kStride];              // first output slot of the tile's digit
-  __shared__ uint32_t sw[NW];
-  __shared__ int s_tile, s_ok;
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  __shared__ int sw[NW];
+  __shared__ int s_ok;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, tile = blockIdx.x;
   const int sh = pass * a.digit_bits;
   const uint32_t B = pass_buckets(a, pass), mask = B - 1;
   const uint32_t lt = (1u << lane) - 1u;
@@ -708,19 +711,7 @@ __global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const u
     for (uint32_t d = t; d < B; d += kTileThreads) cnt[w * kStride + d] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
-  if (t == 0) {
-    s_ok = a.header->status == EWG_OK;
-    s_tile = atomicAdd(&a.counters[pass], 1);
-  }
-  uint32_t tot[kDpt];
-#pragma unroll
-  for (int j = 0; j < kDpt; ++j) {
-    const uint32_t d = t * kDpt + j;
-    tot[j] = d < B ? a.totals[pass * kStride + d] : 0u;
-  }
-  __syncthreads();
-  if (!s_ok) return;
-  const int tile = s_tile;
+  if (t == 0) s_ok = a.header->status == EWG_OK;
   uint32_t key[kTileItems], val[kTileItems];
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
@@ -728,6 +719,31 @@ __global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const u
     key[r] = ks[idx];
     val[r] = vs[idx];
   }
+  // this thread's digits d0 and d0 + 1: keys of each over all tiles (tot) and over the
+  // tiles before this one (pre), from the complete tile histograms of this pass
+  const int d0 = 2 * t;
+  const uint32_t* hist = a.tile_hist + static_cast<long long>(pass) * a.tiles * kStride + d0;
+  uint32_t tot0 = 0, tot1 = 0, pre0 = 0, pre1 = 0;
+  if (static_cast<uint32_t>(d0) < B) {   // B is even: d0 + 1 < B too
+    for (int j0 = 0; j0 < a.tiles; j0 += kBatch) {
+      uint2 v[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i)
+        v[i] = j0 + i < a.tiles ? *reinterpret_cast<const uint2*>(hist + static_cast<long long>(j0 + i) * kStride)
+                                : make_uint2(0u, 0u);
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        tot0 += v[i].x;
+        tot1 += v[i].y;
+        if (j0 + i < tile) {
+          pre0 += v[i].x;
+          pre1 += v[i].y;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;
   uint32_t rank[kTileItems], dig[kTileItems];
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
@@ -740,62 +756,40 @@ __global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const u
     rank[r] = prior + __popc(peers & lt);
     dig[r] = d;
   }
-  __syncthreads();
-  // the tile's count of each digit; cnt becomes the per-warp offsets within the tile
-  uint32_t own[kDpt];
+  // keys of smaller digits over all tiles: an exclusive scan of the totals over the block
+  // (its barriers also complete the ranks in cnt), then cnt -> per-warp offsets in the tile
+  const int below = block_exclusive_scan<kTileThreads, int>(static_cast<int>(tot0 + tot1), SumIntOp(), 0, sw, nullptr);
 #pragma unroll
-  for (int j = 0; j < kDpt; ++j) {
-    const uint32_t d = t * kDpt + j;
-    uint32_t run = 0;
-    if (d < B)
+  for (int j = 0; j < 2; ++j) {
+    const uint32_t d = d0 + j;
+    if (d < B) {
+      uint32_t run = 0;
       for (int w = 0; w < NW; ++w) {
         const uint32_t c = cnt[w * kStride + d];
         cnt[w * kStride + d] = run;
         run += c;
       }
-    own[j] = run;
-  }
-  uint32_t* words = a.sweep + static_cast<long long>(pass) * a.tiles * kStride;
-#pragma unroll
-  for (int j = 0; j < kDpt; ++j) {
-    const uint32_t d = t * kDpt + j;
-    if (d < B) st_relaxed(words + static_cast<long long>(tile) * kStride + d, (tile ? kFlagAgg : kFlagInc) | own[j]);
-  }
-  // digits before d over all keys (totals), plus digit d in the tiles before this one
-  uint32_t sum = 0;
-#pragma unroll
-  for (int j = 0; j < kDpt; ++j) sum += tot[j];
-  uint32_t below = static_cast<uint32_t>(
-      block_exclusive_scan<kTileThreads, int>(static_cast<int>(sum), SumIntOp(), 0, reinterpret_cast<int*>(sw), nullptr));
-  bool ok = true;
-  uint32_t before[kDpt];
-  {
-    uint32_t* w[kDpt];
-    bool act[kDpt];
-#pragma unroll
-    for (int j = 0; j < kDpt; ++j) {
-      w[j] = words + t * kDpt + j;
-      act[j] = t * kDpt + j < B;
-      before[j] = 0;
+      base[d] = static_cast<uint32_t>(below) + (j ? tot0 + pre1 : pre0);
     }
-    if (tile > 0) ok = look_back<16, kDpt>(w, kStride, tile, act, own, before);
   }
-#pragma unroll
-  for (int j = 0; j < kDpt; ++j) {
-    const uint32_t d = t * kDpt + j;
-    if (d < B) base[d] = below + before[j];
-    below += tot[j];
-  }
-  if (__syncthreads_or(!ok)) {
-    if (t == 0) give_up_plan(a);
-    return;
-  }
+  __syncthreads();
+  const bool next = pass + 1 < a.passes;
+  const int nsh = (pass + 1) * a.digit_bits;
+  const uint32_t nmask = next ? pass_buckets(a, pass + 1) - 1u : 0u;
+  uint32_t* nhist = a.tile_hist + static_cast<long long>(pass + 1) * a.tiles * kStride;
 #pragma unroll
   for (int r = 0; r < kTileItems; ++r) {
     const uint32_t dst = base[dig[r]] + cnt[warp * kStride + dig[r]] + rank[r];
-    if (!checked(dst < static_cast<uint32_t>(a.tiles) * kTile, a.header)) continue;
-    kd[dst] = key[r];
-    vd[dst] = val[r];
+    const bool in = checked(dst < static_cast<uint32_t>(a.tiles) * kTile, a.header);
+    if (in) {
+      kd[dst] = key[r];
+      vd[dst] = val[r];
+    }
+    if (next) {   // the next pass's digit of this key, in the tile it now belongs to
+      const uint32_t slot = in ? (dst / kTile) * kStride + ((key[r] >> nsh) & nmask) : 0u;
+      const unsigned peers = __match_any_sync(kFull, slot);
+      if (in && lane == __ffs(peers) - 1) atomicAdd(&nhist[slot], static_cast<uint32_t>(__popc(peers)));
+    }
   }
 }
 
@@ -939,7 +933,6 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   if (a.n <= kHashMaxN) return launch_pdl(plan_hashed_kernel, kHashParts, kHashThreads, kHashSmem, stream, a);
   const int tiles = a.tiles;
   cudaError_t e = launch_pdl(pack_kernel, tiles, kTileThreads, 0, stream, a);
-  if (e == cudaSuccess && a.passes > 0) e = launch_pdl(hist_kernel, tiles, kTileThreads, 0, stream, a);
   const uint32_t* ks = a.keys_a;
   const uint32_t* vs = a.vals_a;
   uint32_t* kd = a.keys_b;
