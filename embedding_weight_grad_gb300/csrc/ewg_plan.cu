@@ -173,20 +173,21 @@ struct Listing {
   int re[ITEMS];
   uint32_t key[ITEMS];
 
-  __device__ void compute(const uint32_t* keys, int n, int s_begin, int rs_seed, int re_seed,
+  // skey: the keys of slots s_begin - 1 .. s_begin + NT * ITEMS, staged in shared memory.
+  __device__ void compute(const uint32_t* skey, int n, int s_begin, int rs_seed, int re_seed,
                           int* swi) {
     const int base = s_begin + threadIdx.x * ITEMS;
     bool head[ITEMS], tail[ITEMS];
     int hmax = -1, tmin = INT_MAX;
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
-      const int s = base + i;
+      const int s = base + i, l = threadIdx.x * ITEMS + i + 1;   // slot s is skey[l]
       head[i] = tail[i] = false;
       key[i] = kPadKey;
       if (s < n) {
-        key[i] = keys[s];
-        head[i] = (s == 0) || keys[s - 1] != key[i];
-        tail[i] = (s == n - 1) || keys[s + 1] != key[i];
+        key[i] = skey[l];
+        head[i] = (s == 0) || skey[l - 1] != key[i];
+        tail[i] = (s == n - 1) || skey[l + 1] != key[i];
         if (head[i]) hmax = max(hmax, s);
         if (tail[i]) tmin = min(tmin, s);
       }
@@ -226,8 +227,9 @@ struct Listing {
   }
 
   // Writes the descriptors of the chunks that start in this thread's slots; `prefix`
-  // is the packed count of the chunks and runs before this thread's slots.
-  __device__ void emit(const PlanArgs& a, const uint32_t* vals, int n, int s_begin,
+  // is the packed count of the chunks and runs before this thread's slots.  sval: the
+  // positions of slots s_begin .. s_begin + NT * ITEMS + NROWS - 1, staged in shared memory.
+  __device__ void emit(const PlanArgs& a, const uint32_t* sval, int n, int s_begin,
                        long long prefix, const EmitBases& b) const {
     const int base = s_begin + threadIdx.x * ITEMS;
     int si = field_short(prefix), li = field_long(prefix), ri = field_runs(prefix);
@@ -250,7 +252,7 @@ struct Listing {
       int p[kNrows];
 #pragma unroll
       for (int k = 0; k < kNrows; ++k) {
-        p[k] = k < len ? static_cast<int>(vals[s + k]) : 0;
+        p[k] = k < len ? static_cast<int>(sval[s - s_begin + k]) : 0;
         if (!checked(p[k] >= 0 && p[k] < n, a.header)) p[k] = 0;
       }
       d[0] = make_int4(p[0], p[1], p[2], p[3]);
@@ -835,14 +837,19 @@ __device__ void tile_seeds(const uint32_t* keys, int n, int s0, int* rs_seed, in
   *re_seed = seeds[1];
 }
 
-// Runs and chunks of the sorted keys, one tile per CTA (tiles in claim order).
+// Runs and chunks of the sorted keys, one tile per CTA (tiles in claim order).  The tile's
+// keys (with one slot on each side) and positions (with the NROWS - 1 slots after it) are
+// staged in shared memory by one coalesced load.
 __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const uint32_t* keys,
                                                             const uint32_t* vals) {
+  __shared__ uint32_t skey[kTile + 2];
+  __shared__ uint32_t sval[kTile + kNrows];
   __shared__ int swi[kTileThreads / 32];
   __shared__ long long sw64[kTileThreads / 32];
   __shared__ int s_tile, s_ok;
   __shared__ uint32_t s_before[3], s_own[3];
   const int t = threadIdx.x;
+  const long long n_pad = static_cast<long long>(a.tiles) * kTile;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
   if (t == 0) {
@@ -851,9 +858,28 @@ __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const ui
   }
   long long bad = 0;
   for (int i = t; i < a.tiles; i += kTileThreads) bad += a.tile_bad[i];
-  bad = block_sum<kTileThreads>(bad, sw64);   // its barriers also publish s_ok and s_tile
+  __syncthreads();
   if (!s_ok) return;
   const int tile = s_tile;
+  const int s0 = tile * kTile;
+  {   // every load in flight at once: the tile body as 16-byte vectors, then the halos
+    static_assert(kTileItems == 8, "two 16-byte vectors per thread");
+    const uint4* kv = reinterpret_cast<const uint4*>(keys + s0) + 2 * t;
+    const uint4* vv = reinterpret_cast<const uint4*>(vals + s0) + 2 * t;
+    const uint4 k0 = kv[0], k1 = kv[1], v0 = vv[0], v1 = vv[1];
+    uint32_t halo = 0u;
+    if (t == 0) halo = s0 > 0 ? keys[s0 - 1] : kPadKey;
+    else if (t == 1) halo = s0 + kTile < n_pad ? keys[s0 + kTile] : kPadKey;
+    else if (t < 2 + kNrows) halo = s0 + kTile + (t - 2) < n_pad ? vals[s0 + kTile + (t - 2)] : 0u;
+    uint32_t* sk = skey + 1 + 8 * t;
+    uint32_t* sv = sval + 8 * t;
+    sk[0] = k0.x, sk[1] = k0.y, sk[2] = k0.z, sk[3] = k0.w, sk[4] = k1.x, sk[5] = k1.y, sk[6] = k1.z, sk[7] = k1.w;
+    sv[0] = v0.x, sv[1] = v0.y, sv[2] = v0.z, sv[3] = v0.w, sv[4] = v1.x, sv[5] = v1.y, sv[6] = v1.z, sv[7] = v1.w;
+    if (t == 0) skey[0] = halo;
+    else if (t == 1) skey[kTile + 1] = halo;
+    else if (t < 2 + kNrows) sval[kTile + (t - 2)] = halo;
+  }
+  bad = block_sum<kTileThreads>(bad, sw64);   // its barriers also complete the staging
   if (bad) {   // nothing is listed; the first tile reports the bad ids
     if (tile == 0 && t == 0) {
       write_header_fields(a, 1, static_cast<int>(bad));
@@ -861,11 +887,10 @@ __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const ui
     }
     return;
   }
-  const int s0 = tile * kTile;
   int rs_seed, re_seed;
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
   Listing<kTileThreads, kTileItems> L;
-  L.compute(keys, a.n, s0, rs_seed, re_seed, swi);
+  L.compute(skey, a.n, s0, rs_seed, re_seed, swi);
   long long tot = 0;
   const long long prefix = block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0, a.skip_key),
                                                                          SumOp(), 0ll, sw64, &tot);
@@ -890,7 +915,7 @@ __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const ui
   eb.short_desc = a.short_base + static_cast<int>(s_before[1]);
   eb.partial = static_cast<int>(s_before[0]);
   eb.run = static_cast<int>(s_before[2]);
-  L.emit(a, vals, a.n, s0, prefix, eb);
+  L.emit(a, sval, a.n, s0, prefix, eb);
   if (tile == a.tiles - 1 && t == 0) {
     write_tables(a, 0, static_cast<int>(s_before[0] + s_own[0]), 0, static_cast<int>(s_before[1] + s_own[1]),
                  a.short_base, static_cast<int>(s_before[2] + s_own[2]), 0);
