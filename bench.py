@@ -170,9 +170,11 @@ class ClockSampler:
 
 # --- our arm ---------------------------------------------------------------------------
 
-def traffic_from_profile(kernel_src_hash: str):
+def traffic_from_profile(kernel_src_hash: str, workload: str):
     """DRAM bytes per apply launch from the committed ncu summary, if it was taken on
-    the current kernel source; None otherwise."""
+    the current kernel source and the same workload; None otherwise."""
+    if workload != "large_vocab":
+        return None
     path = os.path.join(ROOT, "profiles", "apply_kernel_large_vocab.json")
     try:
         with open(path) as f:
@@ -349,7 +351,7 @@ def run_ours(args, w, world, rank, local):
     if rank == 0:
         hbm_peak, peak_kind = peaks()
         achieved = apply_bytes / (apply_mean * 1e-3) / 1e9
-        traffic = traffic_from_profile(kernel_source_hash())
+        traffic = traffic_from_profile(kernel_source_hash(), w.name)
         launches_per_call = kernel_launches_per_call(n, V)
         us = mean_ms * 1e3
         out = {
