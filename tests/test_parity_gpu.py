@@ -134,10 +134,25 @@ def make(n, V, H, gdt=torch.bfloat16, mdt=torch.float32, seed=0, ids=None):
     (5000, 1, 64),             # one token id: a single 5000-row run, no radix pass
     (4100, 2, 128),            # two ids: two long runs
     (12000, 40000, 72),        # mostly single-occurrence runs
-    (140000, 100000, 8),       # more than 64 tiles: the one-CTA scan kernels of the sort
+    (140000, 100000, 8),       # 69 tiles: several histogram batches per sweep, several
+                               # listing look-back rounds
+    (300001, 5000, 8),         # 147 tiles, a ragged last one
 ])
 def test_shapes_and_id_patterns(oracle_mod, n, V, H):
     run_case(oracle_mod, *make(n, V, H, seed=n))
+
+
+def test_four_radix_passes(oracle_mod):
+    """Ids of 28 bits (a table of 2^27 + 5 rows): four 7-bit radix passes, the most the
+    multi-tile plan makes; the ids are drawn so that both ends of the table occur."""
+    V, n, H = (1 << 27) + 5, 20000, 8
+    rng = np.random.default_rng(27)
+    ids = rng.integers(0, V, size=n, dtype=np.int64)
+    ids[:50] = V - 1
+    ids[50:120] = 0
+    ids[120:140] = 1 << 26
+    _, grad, mg = make(n, V, H, torch.bfloat16, torch.bfloat16, seed=27, ids=ids)
+    run_case(oracle_mod, ids, grad, mg)
 
 
 @pytest.mark.parametrize("gdt,mdt", [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
