@@ -128,6 +128,9 @@ def make(n, V, H, gdt=torch.bfloat16, mdt=torch.float32, seed=0, ids=None):
 @pytest.mark.parametrize("n,V,H", [
     (3073, 500, 8),            # fewest tokens, narrowest rows
     (8192, 3000, 264),         # largest single-CTA plan, ragged last column slice
+    (8192, 40, 8192),          # hashed plan, 40 long runs over wide rows (four column tiles)
+    (4000, 300, 8200),         # hashed plan, rows just past four 2048-column tiles
+    (8192, 2, 4096),           # hashed plan, two runs of about 4096 rows each
     (8193, 3000, 1000),        # first multi-CTA plan, ragged tile and slice
     (20000, 129280, 520),      # 17-bit ids, several tiles
     (70001, 1 << 20, 16),      # 20-bit ids (3 radix passes), many tiles
@@ -155,11 +158,22 @@ def test_four_radix_passes(oracle_mod):
     run_case(oracle_mod, ids, grad, mg)
 
 
-@pytest.mark.parametrize("gdt,mdt", [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
-                                     (torch.float32, torch.float32), (torch.float32, torch.bfloat16)])
+DTYPES = [(torch.bfloat16, torch.float32), (torch.bfloat16, torch.bfloat16),
+          (torch.float32, torch.float32), (torch.float32, torch.bfloat16)]
+
+
+@pytest.mark.parametrize("gdt,mdt", DTYPES)
 def test_dtype_matrix(oracle_mod, gdt, mdt):
     ids = workloads.zipf_ids(np.random.default_rng(3), 20000, 1.2, 12000)
     run_case(oracle_mod, *make(12000, 20000, 392, gdt, mdt, seed=5, ids=ids))
+
+
+@pytest.mark.parametrize("gdt,mdt", DTYPES)
+def test_dtype_matrix_hashed_plan(oracle_mod, gdt, mdt):
+    """The four dtype pairs at 8000 tokens (the hashed plan): Zipf ids, so long runs with
+    their folds and single-chunk runs both occur."""
+    ids = workloads.zipf_ids(np.random.default_rng(13), 20000, 1.2, 8000)
+    run_case(oracle_mod, *make(8000, 20000, 392, gdt, mdt, seed=15, ids=ids))
 
 
 def test_int32_ids_and_strided_tensors(oracle_mod):
@@ -183,6 +197,16 @@ def test_runs_at_chunk_boundaries(oracle_mod):
     ids = np.repeat(np.arange(len(lengths)), lengths)
     ids = np.random.default_rng(9).permutation(ids)
     run_case(oracle_mod, *make(ids.size, len(lengths), 136, seed=9, ids=ids))
+
+
+def test_runs_at_chunk_boundaries_hashed_plan(oracle_mod):
+    """The same run lengths plus 30, 31, 40 and 41 rows in 8000 tokens (the hashed plan),
+    the other positions single-row runs of their own ids."""
+    lengths = [1, 9, 10, 11, 19, 20, 21, 30, 31, 40, 41, 101] * 20
+    ids = np.repeat(np.arange(len(lengths)), lengths)
+    ids = np.random.default_rng(19).permutation(ids)
+    ids = np.concatenate([ids, np.arange(1000, 1000 + 8000 - ids.size)])
+    run_case(oracle_mod, *make(ids.size, 9000, 200, seed=19, ids=ids))
 
 
 def test_repeated_calls_accumulate(oracle_mod):
