@@ -231,6 +231,7 @@ int do_apply(const void* grad, int grad_dtype, int64_t grad_row_stride, void* mg
   a.partial = at<float>(ws, L.partial);
   a.partial_cap = static_cast<int>(ewg::max_partial_rows(n));
   a.arrivals = at<int>(ws, L.arrivals);
+  a.parts = n <= ewg::kHashMaxN ? ewg::kHashParts : 1;
   // Only when the plan of the same call runs just before (and every grad row is read):
   // up to kPrefetchBytes of the first grad rows, at most half of them.
   const int64_t grad_row_bytes = H * static_cast<int64_t>(elem_size(grad_dtype));

@@ -648,7 +648,7 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
               sl = h->spin_limit;
     const long long hv = h->num_embeddings;
     int go = status == EWG_OK;
-    if (go && (hn != a.n || hh != a.hidden || hv != a.num_embeddings)) {
+    if (go && (hn != a.n || hh != a.hidden || hv != a.num_embeddings || np != a.parts)) {
       if (blockIdx.x == 0) const_cast<Header*>(h)->status = kStatusInvalid;
       go = 0;
     }
@@ -656,24 +656,26 @@ __global__ void __launch_bounds__(kApplyThreads, kApplyCtasPerSm) apply_kernel(A
     s.epoch = ep;
     s.spin_limit = sl;
   }
-  {   // counts (into prefix, scanned below) and offsets of the three lists
-    constexpr int kEntries = 3 * kMaxParts;
-    constexpr int kPer = (kEntries + kApplyThreads - 1) / kApplyThreads;
+  {   // counts (into prefix, scanned below) and offsets of the three lists, for the
+      // partitions the plan of this size writes (every CTA reads these same lines)
+    constexpr int kPer = (3 * kHashParts + kApplyThreads - 1) / kApplyThreads;
+    static_assert(kHashParts <= kMaxParts, "partition tables");
+    const int parts = a.parts, entries = 3 * parts;
     int cnt[kPer], off[kPer];
 #pragma unroll
     for (int r = 0; r < kPer; ++r) {
       const int i = t + r * kApplyThreads;
-      const int list = i / kMaxParts, p = i - list * kMaxParts;
+      const int list = i / parts, p = i - list * parts;
       const int ct = list == 0 ? kLongCnt : list == 1 ? kShortCnt : kRunCnt;
       const int ot = list == 0 ? kLongOff : list == 1 ? kShortOff : kRunOff;
-      cnt[r] = i < kEntries ? a.tables[ct * kMaxParts + p] : 0;
-      off[r] = i < kEntries ? a.tables[ot * kMaxParts + p] : 0;
+      cnt[r] = i < entries ? a.tables[ct * kMaxParts + p] : 0;
+      off[r] = i < entries ? a.tables[ot * kMaxParts + p] : 0;
     }
 #pragma unroll
     for (int r = 0; r < kPer; ++r) {
       const int i = t + r * kApplyThreads;
-      if (i < kEntries) {
-        const int list = i / kMaxParts, p = i - list * kMaxParts;
+      if (i < entries) {
+        const int list = i / parts, p = i - list * parts;
         s.prefix[list][p] = cnt[r];
         s.offset[list][p] = off[r];
       }

@@ -270,6 +270,7 @@ struct ApplyArgs {
   int* arrivals;           // per long run (at its first partial row): finished chunk parts
   int prefetch_rows;       // grad rows [0, prefetch_rows) pulled into L2 before the kernel
                            // waits on the plan (0: none)
+  int parts;               // partitions the plan of n tokens writes (kHashParts or 1)
 };
 
 // Detail of the last error on the calling thread (read back by ewg_last_error).
