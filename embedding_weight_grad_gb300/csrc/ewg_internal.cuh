@@ -61,6 +61,10 @@ constexpr int kTileThreads = 256;
 constexpr int kTileItems = 8;
 constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
 constexpr int kMaxPasses = 4;                             // ids below 2^31: 31 bits, 9 per pass
+// Look-back words of the listing: each tile's three words sit in a 128-byte line of their
+// own, so the many threads that poll their predecessors spread over L2 slices instead of
+// all polling the same few lines.
+constexpr int kStatusWords = 32;
 
 // Apply kernel.  Bulk copies reach full HBM bandwidth only from about 4 KB up, so an
 // item covers a chunk over a column tile of up to 2048 columns (1024 for an fp32
@@ -188,7 +192,7 @@ inline Layout make_layout(int64_t n, int64_t hidden) {
   L.tile_hist = take(static_cast<size_t>(kMaxPasses) * L.tiles * (1 << kMaxDigitBits) * 4);
   L.ctl = take(static_cast<size_t>(kMaxPasses + 1) * 4);
   L.tile_bad = take(static_cast<size_t>(L.tiles) * 4);
-  L.list_status = take(static_cast<size_t>(L.tiles) * 16);
+  L.list_status = take(static_cast<size_t>(L.tiles) * kStatusWords * 4);
   L.arrivals = take(static_cast<size_t>(max_partial_rows(n)) * 4);
   L.partial = take(static_cast<size_t>(max_partial_rows(n)) * partial_row_floats(hidden) * 4);
   L.total = off;
@@ -247,7 +251,8 @@ struct PlanArgs {
   uint32_t* tile_hist;   // [pass][tile][digit]: keys of each digit in each tile of the pass
   uint32_t* counters;    // [kMaxPasses]: tiles claimed by the listing
   int* tile_bad;         // per tile: ids outside [0, num_embeddings)
-  uint32_t* list_status; // per tile, 4 words: look-back words of long chunks, short chunks, long runs
+  uint32_t* list_status; // per tile, kStatusWords words: look-back words of long chunks, short
+                         // chunks, long runs (the first three)
   int* arrivals;         // per long run, at its first partial row: zeroed here
 };
 

@@ -686,7 +686,7 @@ __global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
     uint32_t* row = a.tile_hist + (static_cast<long long>(p) * a.tiles + tile) * B;
     for (int d = t; d < Bp; d += kTileThreads) row[d] = p == 0 ? h[d] : 0u;
   }
-  if (t < 4) a.list_status[tile * 4 + t] = 0;
+  if (t < 3) a.list_status[static_cast<long long>(tile) * kStatusWords + t] = 0;
   if (tile == 0) {
     if (t <= kMaxPasses) a.counters[t] = 0;
     if (t == 0) a.header->status = EWG_OK;
@@ -897,11 +897,11 @@ __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const ui
   if (t < 3) {   // one look-back chain each: long chunks, short chunks, long-run entries
     const uint32_t own = static_cast<uint32_t>(t == 0 ? field_long(tot) : t == 1 ? field_short(tot) : field_runs(tot));
     uint32_t* word[1] = {a.list_status + t};
-    st_relaxed(word[0] + tile * 4, (tile ? kFlagAgg : kFlagInc) | own);
+    st_relaxed(word[0] + static_cast<long long>(tile) * kStatusWords, (tile ? kFlagAgg : kFlagInc) | own);
     const bool act[1] = {true};
     const uint32_t mine[1] = {own};
     uint32_t before[1] = {0};
-    const bool ok = tile == 0 || look_back<32, 1>(word, 4, tile, act, mine, before);
+    const bool ok = tile == 0 || look_back<32, 1>(word, kStatusWords, tile, act, mine, before);
     s_before[t] = ok ? before[0] : 0xffffffffu;
     s_own[t] = own;
   }
