@@ -39,7 +39,8 @@ def sources():
 
 def _newest_input():
     files = sources() + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cuh")]
-    files.append(os.path.join(ROOT, "include", "ewg.h"))
+    inc = os.path.join(ROOT, "include")
+    files += [os.path.join(inc, f) for f in os.listdir(inc) if f.endswith(".h")]
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 

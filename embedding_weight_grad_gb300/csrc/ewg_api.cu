@@ -9,6 +9,7 @@
 #include <nvtx3/nvToolsExt.h>
 
 #include "ewg.h"
+#include "ewg_debug.h"
 #include "ewg_internal.cuh"
 
 namespace {
@@ -500,6 +501,18 @@ int ewg_accumulate_host(const void* ids_host, int ids_dtype, int64_t num_tokens,
 }
 
 const char* ewg_last_error(void) { return g_last_error.c_str(); }
+
+#ifdef EWG_DEBUG
+int ewg_debug_lookback_probe(void* words, int tile, int poll_limit, int* out, void* stream) {
+  g_last_error.clear();
+  if (!words || !out || tile < 1 || poll_limit < 1)
+    return fail(EWG_ERR_INVALID, "null pointer, tile < 1 or poll_limit < 1");
+  cudaError_t e = ewg::launch_lookback_probe(static_cast<uint32_t*>(words), tile, poll_limit, out,
+                                             static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "look-back probe launch");
+  return EWG_OK;
+}
+#endif
 
 int ewg_version(void) { return 1; }
 

@@ -284,6 +284,10 @@ void set_last_error(const char* msg);
 // Host-side launchers.
 cudaError_t prepare_kernels();   // once per device, before the first launch
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+#ifdef EWG_DEBUG
+// The look-back test probe of the bounds-checking build (see include/ewg_debug.h).
+cudaError_t launch_lookback_probe(uint32_t* words, int tile, int poll_limit, int* out, cudaStream_t stream);
+#endif
 // The apply kernel, chained to its predecessor by programmatic dependent launch.
 cudaError_t launch_apply(const ApplyArgs& a, int grad_bf16, int mg_bf16, int num_sms,
                          cudaStream_t stream);

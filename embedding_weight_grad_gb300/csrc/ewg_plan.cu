@@ -585,10 +585,10 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 // before the first inclusive one; it then adds them from the closest on until a word holds
 // an inclusive sum.  Every tile publishes its aggregate early, so a round usually settles
 // up to K tiles in one or two round trips.  Publishes this tile's inclusive sums.  False if
-// a predecessor published nothing within the poll limit.
+// a predecessor published nothing within poll_limit polls of its word.
 template <int K, int NCH>
 __device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int tile, const bool (&active)[NCH],
-                          const uint32_t (&own)[NCH], uint32_t (&excl)[NCH]) {
+                          const uint32_t (&own)[NCH], uint32_t (&excl)[NCH], int poll_limit = kLookBackPolls) {
 #pragma unroll
   for (int c = 0; c < NCH; ++c) {
     if (!active[c]) continue;
@@ -608,7 +608,7 @@ __device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int ti
           }
         }
         if (!pending) break;
-        if (poll >= kLookBackPolls) return false;
+        if (poll >= poll_limit) return false;
         __nanosleep(32);
 #pragma unroll
         for (int i = 0; i < K; ++i)
@@ -632,6 +632,23 @@ __device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int ti
 }
 
 __device__ void give_up_plan(const PlanArgs& a) { atomicExch(&a.header->status, kStatusTimeout); }
+
+#ifdef EWG_DEBUG
+// Test probe of the look-back (bounds-checking build only): one thread looks back from
+// `tile` over words prepared by the caller, a word of 0 being a predecessor that never
+// publishes, with at most poll_limit polls of a word.  out[0]: 1 if it completed, 0 if it
+// gave up; out[1]: the exclusive sum it found.
+__global__ void lookback_probe_kernel(uint32_t* words, int tile, int poll_limit, int* out) {
+  if (threadIdx.x != 0) return;
+  uint32_t* word[1] = {words};
+  const bool act[1] = {true};
+  const uint32_t mine[1] = {1u};
+  uint32_t before[1] = {0u};
+  const bool ok = look_back<32, 1>(word, 1, tile, act, mine, before, poll_limit);
+  out[0] = ok ? 1 : 0;
+  out[1] = static_cast<int>(before[0]);
+}
+#endif
 
 // Digit width of `pass` (the last pass may take fewer bits).
 __device__ __forceinline__ uint32_t pass_buckets(const PlanArgs& a, int pass) {
@@ -953,6 +970,13 @@ cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem
 }
 
 }  // namespace
+
+#ifdef EWG_DEBUG
+cudaError_t launch_lookback_probe(uint32_t* words, int tile, int poll_limit, int* out, cudaStream_t stream) {
+  lookback_probe_kernel<<<1, 32, 0, stream>>>(words, tile, poll_limit, out);
+  return cudaGetLastError();
+}
+#endif
 
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   if (a.n <= kHashMaxN) return launch_pdl(plan_hashed_kernel, kHashParts, kHashThreads, kHashSmem, stream, a);

@@ -48,6 +48,19 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, n)
 
 
+def test_debug_hooks_only_in_the_checked_build():
+    """include/ewg_debug.h declares test hooks that libewg_debug.so exports and libewg.so
+    does not."""
+    src = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "ewg_debug.h")).read(), flags=re.S)
+    names = sorted(set(re.findall(r"\b(ewg_[a-z_]+)\s*\(", src)))
+    assert names == ["ewg_debug_lookback_probe"]
+    dbg = cuda_build.build(debug=True)
+    nm = lambda path: set(re.findall(r"\bT (ewg_[a-z_]+)\b", subprocess.run(
+        ["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout))
+    assert set(names) <= nm(dbg)
+    assert not set(names) & nm(ewg.library_path())
+
+
 def test_constants_match_binding():
     d = header_defines()
     assert d["EWG_MIN_TOKENS"] == ewg.MIN_TOKENS == 3073

@@ -80,3 +80,38 @@ def chunk_region_offset(L, n, H):
     n_pad = -(-n // 2048) * 2048
     off = up(256) + up(6 * 128 * 4)
     return off + 4 * up(n_pad * 4)
+
+
+def probe(dlib, words, tile, poll_limit):
+    out = torch.full((2,), -1, dtype=torch.int32, device=DEV)
+    dlib.ewg_debug_lookback_probe.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p]
+    assert dlib.ewg_debug_lookback_probe(words.data_ptr(), tile, poll_limit, out.data_ptr(), stream()) == ewg.OK
+    torch.cuda.synchronize()
+    return out.tolist()
+
+
+AGG, INC = 1 << 30, 2 << 30   # word formats of the listing's look-back (include/ewg_debug.h)
+
+
+def test_lookback_sums_its_predecessors(dlib):
+    """40 tiles (two batches of 32 predecessors): tile 0 holds an inclusive sum, the others
+    their own counts; the probe from tile 39 finds the sum of all 39 and publishes its own."""
+    T = 40
+    counts = list(range(1, T))                       # tile j has count j + 1
+    w = torch.tensor([INC | 1] + [AGG | c for c in counts[1:]] + [0], dtype=torch.int64).to(torch.int32).to(DEV)
+    done, excl = probe(dlib, w, T - 1, 1 << 20)
+    assert (done, excl) == (1, sum(counts))
+    assert int(w[T - 1].item()) & 0xffffffff == (INC | (sum(counts) + 1))
+
+
+def test_lookback_gives_up_on_a_predecessor_that_never_publishes(dlib):
+    """Tile 5's word is never published: the probe must end on its own after its poll limit
+    and report that it gave up, without publishing a sum."""
+    T = 40
+    vals = [INC | 1] + [AGG | (j + 1) for j in range(1, T - 1)] + [0]
+    vals[5] = 0
+    w = torch.tensor(vals, dtype=torch.int64).to(torch.int32).to(DEV)
+    done, _ = probe(dlib, w, T - 1, 2000)
+    assert done == 0
+    assert int(w[T - 1].item()) == 0
