@@ -40,3 +40,40 @@ def test_random_configuration(oracle_mod, seed):
     ids, n, V, H, gdt, mdt, ids_dtype = random_case(seed)
     _, grad, mg = make(n, V, H, gdt, mdt, seed=seed, ids=ids)
     run_case(oracle_mod, ids, grad, mg, ids_dtype=ids_dtype)
+
+
+def _pinned(t: torch.Tensor) -> torch.Tensor:
+    return t.cpu().contiguous().pin_memory()
+
+
+@pytest.mark.parametrize("seed", range(24, 42))
+def test_random_configuration_other_entry_points(oracle_mod, seed):
+    """The same random configurations through the other entry points, in turn: one plan
+    applied twice (ewg_plan, then ewg_apply twice: the apply's epoch lets a plan serve
+    repeated calls), a random row range of the table (ewg_accumulate_shard), and ids and
+    grad in pinned host memory (ewg_accumulate_host)."""
+    from test_parity_gpu import assert_same_bits, oracle_expected
+    ids, n, V, H, gdt, mdt, ids_dtype = random_case(seed)
+    _, grad, mg = make(n, V, H, gdt, mdt, seed=seed, ids=ids)
+    ids_d = torch.from_numpy(ids).to(DEV, ids_dtype)
+    before = mg.clone()
+    entry = ["plan_twice", "shard", "host"][seed % 3]
+    if entry == "plan_twice":
+        ws = ewg.new_workspace(n, H, DEV)
+        ewg.plan(ids_d, V, H, ws)
+        ewg.apply(grad, mg, n, ws)
+        ewg.apply(grad, mg, n, ws)
+        assert ewg.read_status(ws) == ewg.OK
+        want = oracle_expected(oracle_mod, ids, grad, oracle_expected(oracle_mod, ids, grad, before))
+        assert_same_bits(mg, want)
+    elif entry == "shard":
+        rng = np.random.default_rng(20_000 + seed)
+        b0 = int(rng.integers(0, V))
+        b1 = int(rng.integers(b0 + 1, V + 1))
+        shard = mg[b0:b1].clone()
+        ewg.accumulate_embedding_wgrad_shard(ids_d, grad, shard, b0, V, check=True)
+        want = oracle_expected(oracle_mod, ids, grad, before)
+        assert_same_bits(shard, want[b0:b1])
+    else:
+        ewg.accumulate_embedding_wgrad_from_host(_pinned(ids_d), _pinned(grad), mg, check=True)
+        assert_same_bits(mg, oracle_expected(oracle_mod, ids, grad, before))
