@@ -103,11 +103,10 @@ int ewg_can_accumulate(const void* ids, int ids_dtype, int64_t num_tokens,
  * Bytes of device workspace that ewg_accumulate / ewg_plan / ewg_apply need for
  * num_tokens tokens of width hidden (an upper bound over every id pattern).  The page
  * has no counterpart: its function allocates its own scratch, while this library leaves
- * every allocation to the caller.  The
- * workspace needs no initialisation and holds no state the caller must keep
- * between calls, except that ewg_apply reads the plan that ewg_plan left in it and
- * ewg_read_status reads the status of the last call.  Returns 0 for sizes outside
- * the supported range.
+ * every allocation to the caller.  The workspace needs no initialisation and holds no
+ * state the caller must keep between calls, except that ewg_apply reads the plan that
+ * ewg_plan left in it and ewg_read_status reads the status of the last call.  Returns 0
+ * for sizes outside the supported range.
  */
 size_t ewg_workspace_bytes(int64_t num_tokens, int64_t hidden);
 
