@@ -51,8 +51,8 @@ enum Table { kLongCnt = 0, kLongOff, kShortCnt, kShortOff, kRunCnt, kRunOff, kTa
 
 // Hashed plan (up to 8192 tokens): one CTA per hash partition of the ids.
 constexpr int kHashParts = 64;
-constexpr int kHashThreads = 512;
-constexpr int kHashItems = 16;
+constexpr int kHashThreads = 1024;
+constexpr int kHashItems = 8;
 constexpr int kHashMaxN = kHashThreads * kHashItems;      // 8192 tokens
 constexpr int kMaxDigitBits = 9;                          // 512 buckets per radix pass
 
