@@ -854,15 +854,19 @@ __device__ void tile_seeds(const uint32_t* keys, int n, int s0, int* rs_seed, in
   *re_seed = seeds[1];
 }
 
+// The listing takes a tile of kTile sorted slots on kListThreads threads, kListItems each.
+constexpr int kListThreads = 512;
+constexpr int kListItems = kTile / kListThreads;
+
 // Runs and chunks of the sorted keys, one tile per CTA (tiles in claim order).  The tile's
 // keys (with one slot on each side) and positions (with the NROWS - 1 slots after it) are
 // staged in shared memory by one coalesced load.
-__global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const uint32_t* keys,
+__global__ void __launch_bounds__(kListThreads) list_kernel(PlanArgs a, const uint32_t* keys,
                                                             const uint32_t* vals) {
   __shared__ uint32_t skey[kTile + 2];
   __shared__ uint32_t sval[kTile + kNrows];
-  __shared__ int swi[kTileThreads / 32];
-  __shared__ long long sw64[kTileThreads / 32];
+  __shared__ int swi[kListThreads / 32];
+  __shared__ long long sw64[kListThreads / 32];
   __shared__ int s_tile, s_ok;
   __shared__ uint32_t s_before[3], s_own[3];
   const int t = threadIdx.x;
@@ -874,29 +878,28 @@ __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const ui
     s_tile = atomicAdd(&a.counters[kMaxPasses], 1);
   }
   long long bad = 0;
-  for (int i = t; i < a.tiles; i += kTileThreads) bad += a.tile_bad[i];
+  for (int i = t; i < a.tiles; i += kListThreads) bad += a.tile_bad[i];
   __syncthreads();
   if (!s_ok) return;
   const int tile = s_tile;
   const int s0 = tile * kTile;
   {   // every load in flight at once: the tile body as 16-byte vectors, then the halos
-    static_assert(kTileItems == 8, "two 16-byte vectors per thread");
-    const uint4* kv = reinterpret_cast<const uint4*>(keys + s0) + 2 * t;
-    const uint4* vv = reinterpret_cast<const uint4*>(vals + s0) + 2 * t;
-    const uint4 k0 = kv[0], k1 = kv[1], v0 = vv[0], v1 = vv[1];
+    static_assert(kListItems == 4, "one 16-byte vector per thread");
+    const uint4 k0 = reinterpret_cast<const uint4*>(keys + s0)[t];
+    const uint4 v0 = reinterpret_cast<const uint4*>(vals + s0)[t];
     uint32_t halo = 0u;
     if (t == 0) halo = s0 > 0 ? keys[s0 - 1] : kPadKey;
     else if (t == 1) halo = s0 + kTile < n_pad ? keys[s0 + kTile] : kPadKey;
     else if (t < 2 + kNrows) halo = s0 + kTile + (t - 2) < n_pad ? vals[s0 + kTile + (t - 2)] : 0u;
-    uint32_t* sk = skey + 1 + 8 * t;
-    uint32_t* sv = sval + 8 * t;
-    sk[0] = k0.x, sk[1] = k0.y, sk[2] = k0.z, sk[3] = k0.w, sk[4] = k1.x, sk[5] = k1.y, sk[6] = k1.z, sk[7] = k1.w;
-    sv[0] = v0.x, sv[1] = v0.y, sv[2] = v0.z, sv[3] = v0.w, sv[4] = v1.x, sv[5] = v1.y, sv[6] = v1.z, sv[7] = v1.w;
+    uint32_t* sk = skey + 1 + 4 * t;
+    uint32_t* sv = sval + 4 * t;
+    sk[0] = k0.x, sk[1] = k0.y, sk[2] = k0.z, sk[3] = k0.w;
+    sv[0] = v0.x, sv[1] = v0.y, sv[2] = v0.z, sv[3] = v0.w;
     if (t == 0) skey[0] = halo;
     else if (t == 1) skey[kTile + 1] = halo;
     else if (t < 2 + kNrows) sval[kTile + (t - 2)] = halo;
   }
-  bad = block_sum<kTileThreads>(bad, sw64);   // its barriers also complete the staging
+  bad = block_sum<kListThreads>(bad, sw64);   // its barriers also complete the staging
   if (bad) {   // nothing is listed; the first tile reports the bad ids
     if (tile == 0 && t == 0) {
       write_header_fields(a, 1, static_cast<int>(bad));
@@ -906,10 +909,10 @@ __global__ void __launch_bounds__(kTileThreads) list_kernel(PlanArgs a, const ui
   }
   int rs_seed, re_seed;
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
-  Listing<kTileThreads, kTileItems> L;
+  Listing<kListThreads, kListItems> L;
   L.compute(skey, a.n, s0, rs_seed, re_seed, swi);
   long long tot = 0;
-  const long long prefix = block_exclusive_scan<kTileThreads, long long>(L.counts(a.n, s0, a.skip_key),
+  const long long prefix = block_exclusive_scan<kListThreads, long long>(L.counts(a.n, s0, a.skip_key),
                                                                          SumOp(), 0ll, sw64, &tot);
   if (t < 3) {   // one look-back chain each: long chunks, short chunks, long-run entries
     const uint32_t own = static_cast<uint32_t>(t == 0 ? field_long(tot) : t == 1 ? field_short(tot) : field_runs(tot));
@@ -995,7 +998,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
     ks = nk;
     vs = nv;
   }
-  if (e == cudaSuccess) e = launch_pdl(list_kernel, tiles, kTileThreads, 0, stream, a, ks, vs);
+  if (e == cudaSuccess) e = launch_pdl(list_kernel, tiles, kListThreads, 0, stream, a, ks, vs);
   return e;
 }
 
