@@ -655,26 +655,30 @@ __device__ __forceinline__ uint32_t pass_buckets(const PlanArgs& a, int pass) {
   return 1u << min(a.digit_bits, a.id_bits - pass * a.digit_bits);
 }
 
-__global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
+// The packing takes a tile of kTile ids on kPackThreads threads, kPackItems each.
+constexpr int kPackThreads = 1024;
+constexpr int kPackItems = kTile / kPackThreads;
+
+__global__ void __launch_bounds__(kPackThreads) pack_kernel(PlanArgs a) {
   constexpr int B = 1 << kMaxDigitBits;
-  __shared__ long long sw64[kTileThreads / 32];
+  __shared__ long long sw64[kPackThreads / 32];
   __shared__ uint32_t h[B];
   const int t = threadIdx.x, lane = t & 31, tile = blockIdx.x;
-  for (int d = t; d < B; d += kTileThreads) h[d] = 0;
+  for (int d = t; d < B; d += kPackThreads) h[d] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
   int bad = 0;
-  long long raw[kTileItems];
+  long long raw[kPackItems];
 #pragma unroll
-  for (int r = 0; r < kTileItems; ++r) {
-    const int i = tile * kTile + r * kTileThreads + t;
+  for (int r = 0; r < kPackItems; ++r) {
+    const int i = tile * kTile + r * kPackThreads + t;
     raw[r] = i < a.n ? load_id(a.ids, a.ids_int64, i) : 0;
   }
   __syncthreads();   // h is clear
   const uint32_t mask0 = a.passes ? pass_buckets(a, 0) - 1u : 0u;
 #pragma unroll
-  for (int r = 0; r < kTileItems; ++r) {
-    const int i = tile * kTile + r * kTileThreads + t;
+  for (int r = 0; r < kPackItems; ++r) {
+    const int i = tile * kTile + r * kPackThreads + t;
     uint32_t k = kPadKey;
     if (i < a.n) {
       if (raw[r] < 0 || raw[r] >= a.num_embeddings) {
@@ -694,14 +698,14 @@ __global__ void __launch_bounds__(kTileThreads) pack_kernel(PlanArgs a) {
       if (lane == __ffs(peers) - 1) atomicAdd(&h[d], static_cast<uint32_t>(__popc(peers)));
     }
   }
-  bad = static_cast<int>(block_sum<kTileThreads>(bad, sw64));   // its barriers also complete h
+  bad = static_cast<int>(block_sum<kPackThreads>(bad, sw64));   // its barriers also complete h
   if (t == 0) a.tile_bad[tile] = bad;
   // this tile's histogram of the first pass; its rows of the later passes start at zero
   // (the sweep before each of them counts into them)
   for (int p = 0; p < a.passes; ++p) {
     const int Bp = static_cast<int>(pass_buckets(a, p));
     uint32_t* row = a.tile_hist + (static_cast<long long>(p) * a.tiles + tile) * B;
-    for (int d = t; d < Bp; d += kTileThreads) row[d] = p == 0 ? h[d] : 0u;
+    for (int d = t; d < Bp; d += kPackThreads) row[d] = p == 0 ? h[d] : 0u;
   }
   if (t < 3) a.list_status[static_cast<long long>(tile) * kStatusWords + t] = 0;
   if (tile == 0) {
@@ -984,7 +988,7 @@ cudaError_t launch_lookback_probe(uint32_t* words, int tile, int poll_limit, int
 cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   if (a.n <= kHashMaxN) return launch_pdl(plan_hashed_kernel, kHashParts, kHashThreads, kHashSmem, stream, a);
   const int tiles = a.tiles;
-  cudaError_t e = launch_pdl(pack_kernel, tiles, kTileThreads, 0, stream, a);
+  cudaError_t e = launch_pdl(pack_kernel, tiles, kPackThreads, 0, stream, a);
   const uint32_t* ks = a.keys_a;
   const uint32_t* vs = a.vals_a;
   uint32_t* kd = a.keys_b;
