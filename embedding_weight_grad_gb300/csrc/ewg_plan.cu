@@ -714,14 +714,19 @@ __global__ void __launch_bounds__(kPackThreads) pack_kernel(PlanArgs a) {
   }
 }
 
+// The sweep takes a tile of kTile keys on kSweepThreads threads, kSweepItems each; each
+// thread owns one digit of the histogram.
+constexpr int kSweepThreads = 1 << kMaxDigitBits;
+constexpr int kSweepItems = kTile / kSweepThreads;
+
 // One stable LSD radix pass: (ks, vs) -> (kd, vd), ordered by the digit of `pass`.
-__global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const uint32_t* ks,
-                                                             const uint32_t* vs, uint32_t* kd,
-                                                             uint32_t* vd, int pass) {
-  constexpr int NW = kTileThreads / 32;
+__global__ void __launch_bounds__(kSweepThreads) sweep_kernel(PlanArgs a, const uint32_t* ks,
+                                                              const uint32_t* vs, uint32_t* kd,
+                                                              uint32_t* vd, int pass) {
+  constexpr int NW = kSweepThreads / 32;
   constexpr int kStride = 1 << kMaxDigitBits;
   constexpr int kBatch = 32;                      // histogram rows loaded together
-  static_assert(kStride == 2 * kTileThreads, "each thread owns two consecutive digits");
+  static_assert(kStride == kSweepThreads, "each thread owns one digit");
   __shared__ uint32_t cnt[NW * kStride];          // [warp][digit]
   __shared__ uint32_t base[kStride];              // first output slot of the tile's digit
   __shared__ int sw[NW];
@@ -731,69 +736,60 @@ __global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const u
   const uint32_t B = pass_buckets(a, pass), mask = B - 1;
   const uint32_t lt = (1u << lane) - 1u;
   for (int w = 0; w < NW; ++w)
-    for (uint32_t d = t; d < B; d += kTileThreads) cnt[w * kStride + d] = 0;
+    if (static_cast<uint32_t>(t) < B) cnt[w * kStride + t] = 0;
   ptx::pdl_wait_prior_grid();
   ptx::pdl_launch_dependents();
   if (t == 0) s_ok = a.header->status == EWG_OK;
-  uint32_t key[kTileItems], val[kTileItems];
+  uint32_t key[kSweepItems], val[kSweepItems];
 #pragma unroll
-  for (int r = 0; r < kTileItems; ++r) {
-    const int idx = tile * kTile + warp * (32 * kTileItems) + r * 32 + lane;
+  for (int r = 0; r < kSweepItems; ++r) {
+    const int idx = tile * kTile + warp * (32 * kSweepItems) + r * 32 + lane;
     key[r] = ks[idx];
     val[r] = vs[idx];
   }
-  // this thread's digits d0 and d0 + 1: keys of each over all tiles (tot) and over the
-  // tiles before this one (pre), from the complete tile histograms of this pass
-  const int d0 = 2 * t;
-  const uint32_t* hist = a.tile_hist + static_cast<long long>(pass) * a.tiles * kStride + d0;
-  uint32_t tot0 = 0, tot1 = 0, pre0 = 0, pre1 = 0;
-  if (static_cast<uint32_t>(d0) < B) {   // B is even: d0 + 1 < B too
+  // this thread's digit d: keys of it over all tiles (tot) and over the tiles before this
+  // one (pre), from the complete tile histograms of this pass
+  const int d = t;
+  const uint32_t* hist = a.tile_hist + static_cast<long long>(pass) * a.tiles * kStride + d;
+  uint32_t tot = 0, pre = 0;
+  if (static_cast<uint32_t>(d) < B) {
     for (int j0 = 0; j0 < a.tiles; j0 += kBatch) {
-      uint2 v[kBatch];
+      uint32_t v[kBatch];
 #pragma unroll
       for (int i = 0; i < kBatch; ++i)
-        v[i] = j0 + i < a.tiles ? *reinterpret_cast<const uint2*>(hist + static_cast<long long>(j0 + i) * kStride)
-                                : make_uint2(0u, 0u);
+        v[i] = j0 + i < a.tiles ? hist[static_cast<long long>(j0 + i) * kStride] : 0u;
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
-        tot0 += v[i].x;
-        tot1 += v[i].y;
-        if (j0 + i < tile) {
-          pre0 += v[i].x;
-          pre1 += v[i].y;
-        }
+        tot += v[i];
+        if (j0 + i < tile) pre += v[i];
       }
     }
   }
   __syncthreads();
   if (!s_ok) return;
-  uint32_t rank[kTileItems], dig[kTileItems];
+  uint32_t rank[kSweepItems], dig[kSweepItems];
 #pragma unroll
-  for (int r = 0; r < kTileItems; ++r) {
-    const uint32_t d = (key[r] >> sh) & mask;
-    const unsigned peers = __match_any_sync(kFull, d);
-    const uint32_t prior = cnt[warp * kStride + d];
+  for (int r = 0; r < kSweepItems; ++r) {
+    const uint32_t dd = (key[r] >> sh) & mask;
+    const unsigned peers = __match_any_sync(kFull, dd);
+    const uint32_t prior = cnt[warp * kStride + dd];
     __syncwarp();
-    if (lane == 31 - __clz(peers)) cnt[warp * kStride + d] = prior + __popc(peers);
+    if (lane == 31 - __clz(peers)) cnt[warp * kStride + dd] = prior + __popc(peers);
     __syncwarp();
     rank[r] = prior + __popc(peers & lt);
-    dig[r] = d;
+    dig[r] = dd;
   }
   // keys of smaller digits over all tiles: an exclusive scan of the totals over the block
   // (its barriers also complete the ranks in cnt), then cnt -> per-warp offsets in the tile
-  const int below = block_exclusive_scan<kTileThreads, int>(static_cast<int>(tot0 + tot1), SumIntOp(), 0, sw, nullptr);
-#pragma unroll
-  for (int j = 0; j < 2; ++j) {
-    const uint32_t d = d0 + j;
-    if (d < B) {
-      uint32_t run = 0;
-      for (int w = 0; w < NW; ++w) {
-        const uint32_t c = cnt[w * kStride + d];
-        cnt[w * kStride + d] = run;
-        run += c;
-      }
-      base[d] = static_cast<uint32_t>(below) + (j ? tot0 + pre1 : pre0);
+  const int below = block_exclusive_scan<kSweepThreads, int>(static_cast<int>(tot), SumIntOp(), 0, sw, nullptr);
+  if (static_cast<uint32_t>(d) < B) {
+    uint32_t run = 0;
+    for (int w = 0; w < NW; ++w) {
+      const uint32_t c = cnt[w * kStride + d];
+      cnt[w * kStride + d] = run;
+      run += c;
     }
+    base[d] = static_cast<uint32_t>(below) + pre;
   }
   __syncthreads();
   const bool next = pass + 1 < a.passes;
@@ -801,7 +797,7 @@ __global__ void __launch_bounds__(kTileThreads) sweep_kernel(PlanArgs a, const u
   const uint32_t nmask = next ? pass_buckets(a, pass + 1) - 1u : 0u;
   uint32_t* nhist = a.tile_hist + static_cast<long long>(pass + 1) * a.tiles * kStride;
 #pragma unroll
-  for (int r = 0; r < kTileItems; ++r) {
+  for (int r = 0; r < kSweepItems; ++r) {
     const uint32_t dst = base[dig[r]] + cnt[warp * kStride + dig[r]] + rank[r];
     const bool in = checked(dst < static_cast<uint32_t>(a.tiles) * kTile, a.header);
     if (in) {
@@ -994,7 +990,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
   uint32_t* kd = a.keys_b;
   uint32_t* vd = a.vals_b;
   for (int pass = 0; pass < a.passes && e == cudaSuccess; ++pass) {
-    e = launch_pdl(sweep_kernel, tiles, kTileThreads, 0, stream, a, ks, vs, kd, vd, pass);
+    e = launch_pdl(sweep_kernel, tiles, kSweepThreads, 0, stream, a, ks, vs, kd, vd, pass);
     const uint32_t* nk = kd;
     const uint32_t* nv = vd;
     kd = const_cast<uint32_t*>(ks);
