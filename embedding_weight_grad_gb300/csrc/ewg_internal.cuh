@@ -56,10 +56,9 @@ constexpr int kHashItems = 8;
 constexpr int kHashMaxN = kHashThreads * kHashItems;      // 8192 tokens
 constexpr int kMaxDigitBits = 9;                          // 512 buckets per radix pass
 
-// Multi-tile plan.
-constexpr int kTileThreads = 256;
-constexpr int kTileItems = 8;
-constexpr int kTile = kTileThreads * kTileItems;          // 2048 keys per tile
+// Multi-tile plan: tiles of kTile keys, one CTA each (each kernel picks its own threads
+// per tile).
+constexpr int kTile = 2048;
 constexpr int kMaxPasses = 4;                             // ids below 2^31: 31 bits, 9 per pass
 // Look-back words of the listing: each tile's three words sit in a 128-byte line of their
 // own, so the many threads that poll their predecessors spread over L2 slices instead of
