@@ -291,9 +291,10 @@ struct Producer {
 
   // Waits until every consumer warp that handled a chunk item of the run has stored its
   // partial columns: C chunks x Tl column tiles x kConsumerWarps arrivals.  Lane 0 polls
-  // (at most spin_limit times, and it stops early once this CTA or any other has given
-  // up); then every lane acquires the counter itself, so its later bulk copies of the
-  // partial rows (async proxy) come after the rows' generic-proxy stores.
+  // with acquire loads (at most spin_limit times, and it stops early once this CTA or any
+  // other has given up), then orders its later bulk copies of the partial rows (async
+  // proxy) after the rows' generic-proxy stores.  Lane 0 alone copies partial rows; the
+  // other copy of a fold, the main_grad segment, reads nothing the run's chunks write.
   __device__ bool wait_run(int prow0, int target) {
     const int* cnt = a.arrivals + prow0;
     const volatile int* status = &a.header->status;
@@ -309,13 +310,9 @@ struct Producer {
         if ((i & 63) == 63 && (s.abort || *status == kStatusTimeout)) break;
         __nanosleep(64);
       }
+      if (got) asm volatile("fence.proxy.async.global;" ::: "memory");
     }
-    if (!__shfl_sync(kFull, got, 0)) return false;
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
-    (void)v;
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-    return true;
+    return __shfl_sync(kFull, got, 0) != 0;
   }
 
   // One fold: a column slice (the whole 512-column group, or the entry's 1/split of it)
@@ -599,9 +596,10 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
         }
       }
       if (it.kind == kLongChunk) {   // publish this warp's partial columns to the fold
-        __threadfence();
+        // every lane's stores precede lane 0's release add (the warp barrier orders them
+        // first); the fold's acquire load of the counter pairs with it
         __syncwarp();
-        if (lane == 0) atomicAdd(a.arrivals + (it.prow - it.flags), 1);
+        if (lane == 0) ptx::red_release_add(a.arrivals + (it.prow - it.flags), 1);
       }
     }
     __syncwarp();
