@@ -556,7 +556,7 @@ __device__ void consume(const ApplyArgs& a, Smem& s, const unsigned char* ring) 
       if (c < it.cols) {
         if (it.flags & 1) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) total[e] = 0.0f;   // "in order starting from 0"
+          for (int e = 0; e < 8; ++e) total[e] = 0.0f;   // the combine starts from 0
         }
         for (int k = 0; k < it.rows; ++k) add_row<false>(total, base + k * row_bytes + c * 4);
         if (it.flags & 2)

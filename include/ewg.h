@@ -224,9 +224,9 @@ int ewg_accumulate_host(const void* ids_host, int ids_dtype, int64_t num_tokens,
 #define EWG_STATIC_SCRATCH_BYTES ((size_t)64 << 20)
 
 /*
- * ewg_accumulate without a caller workspace and without any allocation.  Neither the
- * page nor the paper behind it has a counterpart: this is an addition for callers that
- * cannot allocate.
+ * ewg_accumulate without a caller workspace and without any allocation.  The page
+ * (Megatron Core API docs, core.fusions.fused_embedding_wgrad) has no counterpart: this
+ * is an addition for callers that cannot allocate.
  *
  * For callers that cannot allocate device memory when the gradient is accumulated:
  * code running under a fixed-pool or custom allocator that must not grow, and runtimes
