@@ -16,9 +16,10 @@
 // Above 8192 tokens (multi-tile path): an LSD radix sort over the id bits only (keys
 // arrive in position order and every pass is stable, so positions stay ascending in
 // each run without passes of their own) over tiles of 2048 keys, one kernel per pass:
-// each tile ranks its keys and finds where its digits start by decoupled look-back over
-// the tiles before it (a single sweep per pass, in the manner of a "onesweep" radix
-// sort), then one listing kernel that places its chunks by the same look-back.
+// each tile ranks its keys and finds where its digits start from the digit histograms of
+// all tiles, which the kernel before it completed (a single sweep per pass, in the
+// manner of a "onesweep" radix sort), then one listing kernel that places its chunks by
+// decoupled look-back over the tiles before it.
 //
 // The listing gives every sorted slot s its run's first slot rs and last slot re.
 // Slot s starts a chunk when (s - rs) % NROWS == 0.
@@ -566,7 +567,7 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
 constexpr uint32_t kFlagAgg = 1u << 30;   // the word holds the tile's own count
 constexpr uint32_t kFlagInc = 2u << 30;   // ... the sum over the tile and all before it
 constexpr uint32_t kCountMask = kFlagAgg - 1u;
-constexpr int kLookBackPolls = 1 << 20;   // polls of one predecessor's word (about 0.5 s)
+constexpr int kLookBackPolls = 1 << 20;   // poll rounds of one look-back (about 0.5 s)
 
 __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -578,75 +579,61 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
   return v;
 }
 
-// Look-back over NCH chains of words at once (chain c: tile j's word at word[c] + j *
-// stride).  This tile has published its own counts as aggregates (or, as tile 0, as
-// inclusive sums).  Each round loads the words of the K closest predecessors not yet
-// summed, all in flight together, and polls again, together, those not yet published
-// before the first inclusive one; it then adds them from the closest on until a word holds
-// an inclusive sum.  Every tile publishes its aggregate early, so a round usually settles
-// up to K tiles in one or two round trips.  Publishes this tile's inclusive sums.  False if
-// a predecessor published nothing within poll_limit polls of its word.
-template <int K, int NCH>
-__device__ bool look_back(uint32_t* const (&word)[NCH], long long stride, int tile, const bool (&active)[NCH],
-                          const uint32_t (&own)[NCH], uint32_t (&excl)[NCH], int poll_limit = kLookBackPolls) {
-#pragma unroll
-  for (int c = 0; c < NCH; ++c) {
-    if (!active[c]) continue;
-    uint32_t sum = 0;
-    for (int hi = tile; hi > 0;) {
-      const int m = min(hi, K);
-      uint32_t v[K];
-#pragma unroll
-      for (int i = 0; i < K; ++i) v[i] = i < m ? ld_relaxed(word[c] + (hi - 1 - i) * stride) : kFlagInc;
-      for (int poll = 0;; ++poll) {
-        bool pending = false, inc = false;   // an unpublished word before the first inclusive
-#pragma unroll
-        for (int i = 0; i < K; ++i) {
-          if (i < m && !inc && !pending) {
-            pending = !(v[i] & ~kCountMask);
-            inc = (v[i] & kFlagInc) != 0;
-          }
-        }
-        if (!pending) break;
-        if (poll >= poll_limit) return false;
-        __nanosleep(32);
-#pragma unroll
-        for (int i = 0; i < K; ++i)
-          if (i < m && !(v[i] & ~kCountMask)) v[i] = ld_relaxed(word[c] + (hi - 1 - i) * stride);
-      }
-      bool stop = false;
-#pragma unroll
-      for (int i = 0; i < K; ++i) {
-        if (i < m && !stop) {
-          sum += v[i] & kCountMask;
-          stop = (v[i] & kFlagInc) != 0;
-        }
-      }
-      if (stop) break;
-      hi -= m;
+// Decoupled look-back by one whole warp over one chain of words (tile j's word at word +
+// j * stride).  The tile has already published its own count (as tile 0, an inclusive
+// sum).  Each round loads the words of the up to 32 closest predecessors not yet summed,
+// one per lane, all in flight together; re-polls together the ones not yet published
+// before the closest inclusive word; then adds by a warp reduction the counts from the
+// closest predecessor back to that inclusive word, or all of them when there is none and
+// the next 32 follow.  So each round costs one or two round trips whatever the number of
+// predecessors.  Publishes this tile's inclusive sum and gives every lane the exclusive
+// sum in *excl.  False (nothing published) if a predecessor published nothing within
+// poll_limit polls.
+__device__ bool warp_look_back(uint32_t* word, long long stride, int tile, uint32_t own, uint32_t* excl,
+                               int poll_limit = kLookBackPolls) {
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  uint32_t sum = 0;
+  for (int hi = tile; hi > 0;) {
+    const int m = min(hi, 32);
+    const bool valid = lane < m;
+    uint32_t* w = word + static_cast<long long>(hi - 1 - lane) * stride;   // read only if valid
+    uint32_t v = valid ? ld_relaxed(w) : kFlagAgg;   // a lane past the predecessors: count 0
+    unsigned inc, need;   // lanes holding inclusive sums; lanes up to the closest of them
+    for (int poll = 0;; ++poll) {
+      inc = __ballot_sync(kFull, (v & kFlagInc) != 0);
+      const unsigned unpub = __ballot_sync(kFull, (v & ~kCountMask) == 0);
+      need = inc ? (inc & (0u - inc)) * 2u - 1u : kFull;
+      if (!(unpub & need)) break;
+      if (poll >= poll_limit) return false;
+      __nanosleep(32);
+      if ((unpub & need) >> lane & 1u) v = ld_relaxed(w);
     }
-    st_relaxed(word[c] + tile * stride, kFlagInc | (sum + own[c]));
-    excl[c] = sum;
+    uint32_t x = (need >> lane & 1u) ? (v & kCountMask) : 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(kFull, x, o);
+    sum += x;
+    if (inc) break;   // the closest inclusive word ended the sum
+    hi -= m;
   }
+  if (lane == 0) st_relaxed(word + static_cast<long long>(tile) * stride, kFlagInc | (sum + own));
+  *excl = sum;
   return true;
 }
 
 __device__ void give_up_plan(const PlanArgs& a) { atomicExch(&a.header->status, kStatusTimeout); }
 
 #ifdef EWG_DEBUG
-// Test probe of the look-back (bounds-checking build only): one thread looks back from
+// Test probe of the look-back (bounds-checking build only): one warp looks back from
 // `tile` over words prepared by the caller, a word of 0 being a predecessor that never
-// publishes, with at most poll_limit polls of a word.  out[0]: 1 if it completed, 0 if it
-// gave up; out[1]: the exclusive sum it found.
+// publishes, with at most poll_limit polls.  out[0]: 1 if it completed, 0 if it gave up;
+// out[1]: the exclusive sum it found.
 __global__ void lookback_probe_kernel(uint32_t* words, int tile, int poll_limit, int* out) {
-  if (threadIdx.x != 0) return;
-  uint32_t* word[1] = {words};
-  const bool act[1] = {true};
-  const uint32_t mine[1] = {1u};
-  uint32_t before[1] = {0u};
-  const bool ok = look_back<32, 1>(word, 1, tile, act, mine, before, poll_limit);
-  out[0] = ok ? 1 : 0;
-  out[1] = static_cast<int>(before[0]);
+  uint32_t before = 0;
+  const bool ok = warp_look_back(words, 1, tile, 1u, &before, poll_limit);
+  if (threadIdx.x == 0) {
+    out[0] = ok ? 1 : 0;
+    out[1] = static_cast<int>(before);
+  }
 }
 #endif
 
@@ -914,16 +901,17 @@ __global__ void __launch_bounds__(kListThreads) list_kernel(PlanArgs a, const ui
   long long tot = 0;
   const long long prefix = block_exclusive_scan<kListThreads, long long>(L.counts(a.n, s0, a.skip_key),
                                                                          SumOp(), 0ll, sw64, &tot);
-  if (t < 3) {   // one look-back chain each: long chunks, short chunks, long-run entries
-    const uint32_t own = static_cast<uint32_t>(t == 0 ? field_long(tot) : t == 1 ? field_short(tot) : field_runs(tot));
-    uint32_t* word[1] = {a.list_status + t};
-    st_relaxed(word[0] + static_cast<long long>(tile) * kStatusWords, (tile ? kFlagAgg : kFlagInc) | own);
-    const bool act[1] = {true};
-    const uint32_t mine[1] = {own};
-    uint32_t before[1] = {0};
-    const bool ok = tile == 0 || look_back<32, 1>(word, kStatusWords, tile, act, mine, before);
-    s_before[t] = ok ? before[0] : 0xffffffffu;
-    s_own[t] = own;
+  if (t < 3 * 32) {   // one look-back chain per warp: long chunks, short chunks, long-run entries
+    const int c = t >> 5;
+    const uint32_t own = static_cast<uint32_t>(c == 0 ? field_long(tot) : c == 1 ? field_short(tot) : field_runs(tot));
+    uint32_t* word = a.list_status + c;
+    if ((t & 31) == 0) st_relaxed(word + static_cast<long long>(tile) * kStatusWords, (tile ? kFlagAgg : kFlagInc) | own);
+    uint32_t before = 0;
+    const bool ok = tile == 0 || warp_look_back(word, kStatusWords, tile, own, &before);
+    if ((t & 31) == 0) {
+      s_before[c] = ok ? before : 0xffffffffu;
+      s_own[c] = own;
+    }
   }
   __syncthreads();
   if (s_before[0] == 0xffffffffu || s_before[1] == 0xffffffffu || s_before[2] == 0xffffffffu) {

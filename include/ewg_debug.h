@@ -10,12 +10,12 @@ extern "C" {
 #endif
 
 /*
- * Runs the listing's decoupled look-back once, from tile `tile`, on one thread of one CTA,
+ * Runs the listing's decoupled look-back once, from tile `tile`, on one warp of one CTA,
  * over `words` (device memory, tile + 1 uint32 words, one per tile; the caller owns it):
  * word j holds 0 (tile j has not published), (1 << 30) | count (its own count) or
  * (2 << 30) | count (the sum over it and every tile before it).  The probe sums the
- * predecessors' counts back to the first word that holds a sum, polling an unpublished
- * word at most poll_limit times, then publishes word[tile] = (2 << 30) | (sum + 1).
+ * predecessors' counts back to the first word that holds a sum, re-polling unpublished
+ * words at most poll_limit times, then publishes word[tile] = (2 << 30) | (sum + 1).
  * Writes out[0] = 1 if it completed and 0 if it gave up on an unpublished word, and
  * out[1] = the sum it found (device memory, two ints).  Stream-ordered on `stream`.
  * Returns EWG_ERR_INVALID for null pointers, tile < 1 or poll_limit < 1, EWG_ERR_CUDA if
