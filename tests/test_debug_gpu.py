@@ -115,3 +115,31 @@ def test_lookback_gives_up_on_a_predecessor_that_never_publishes(dlib):
     done, _ = probe(dlib, w, T - 1, 2000)
     assert done == 0
     assert int(w[T - 1].item()) == 0
+
+
+def test_lookback_stops_at_the_closest_inclusive_word(dlib):
+    """Tile 20 already holds an inclusive sum: the probe from tile 39 adds tiles 38..21 to
+    it and needs nothing older, so an older word that was never published (tile 10) does
+    not hold it up."""
+    T = 40
+    vals = [AGG | (j + 1) for j in range(T - 1)] + [0]
+    vals[0] = INC | 1
+    vals[20] = INC | 1000
+    vals[10] = 0
+    w = torch.tensor(vals, dtype=torch.int64).to(torch.int32).to(DEV)
+    done, excl = probe(dlib, w, T - 1, 2000)
+    assert (done, excl) == (1, 1000 + sum(range(22, 40)))
+    assert int(w[T - 1].item()) & 0xffffffff == (INC | (1000 + sum(range(22, 40)) + 1))
+
+
+@pytest.mark.parametrize("inc_at", [0, 31, 32, 64, 97])
+def test_lookback_over_several_batches(dlib, inc_at):
+    """100 predecessors, four batches of up to 32, with the closest inclusive word at
+    each batch edge and inside a batch: the sum runs from tile 99 back to that word."""
+    T = 101
+    vals = [AGG | (3 * j + 1) for j in range(T - 1)] + [0]
+    vals[inc_at] = INC | 7
+    w = torch.tensor(vals, dtype=torch.int64).to(torch.int32).to(DEV)
+    done, excl = probe(dlib, w, T - 1, 1 << 20)
+    want = 7 + sum(3 * j + 1 for j in range(inc_at + 1, T - 1))
+    assert (done, excl) == (1, want)
