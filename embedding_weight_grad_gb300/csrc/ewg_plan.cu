@@ -596,7 +596,7 @@ __device__ bool warp_look_back(uint32_t* word, long long stride, int tile, uint3
   for (int hi = tile; hi > 0;) {
     const int m = min(hi, 32);
     const bool valid = lane < m;
-    uint32_t* w = word + static_cast<long long>(hi - 1 - lane) * stride;   // read only if valid
+    uint32_t* w = word + static_cast<long long>(valid ? hi - 1 - lane : hi - 1) * stride;
     uint32_t v = valid ? ld_relaxed(w) : kFlagAgg;   // a lane past the predecessors: count 0
     unsigned inc, need;   // lanes holding inclusive sums; lanes up to the closest of them
     for (int poll = 0;; ++poll) {
