@@ -328,7 +328,37 @@ constexpr int kInRankShift = 13, kLastShift = 18, kGroupCntShift = 23;
 static_assert(kTableMax <= (1 << kRankShift) && kHashMaxN <= (1 << (32 - kRankShift)),
               "slot and rank must pack into one word");
 constexpr size_t kHashSmem =
-    static_cast<size_t>(2) * kHashMaxN * 4 + static_cast<size_t>(3) * kTableMax * 4;
+    static_cast<size_t>(2) * kHashMaxN * 4 + static_cast<size_t>(4) * kTableMax * 4;
+constexpr int kListWarps = kHashWarps - 1;     // warps that list the runs while warp 0 ranks
+
+// Exclusive sum over the threads of warps 1..kListWarps of the block, synchronised by
+// named barrier 1 (warp 0 does other work meanwhile); *total = the sum over all of them.
+__device__ long long list_warps_exclusive_sum(long long v, long long* sw, long long* total) {
+  const int lane = threadIdx.x & 31, w = static_cast<int>(threadIdx.x >> 5) - 1;
+  constexpr int kCount = kListWarps * 32;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFull, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sw[w] = x;
+  asm volatile("bar.sync 1, %0;" ::"n"(kCount) : "memory");
+  if (w == 0) {
+    long long q = lane < kListWarps ? sw[lane] : 0ll;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(kFull, q, o);
+      if (lane >= o) q += y;
+    }
+    if (lane < kListWarps) sw[lane] = q;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kCount) : "memory");
+  const long long before_warp = w > 0 ? sw[w - 1] : 0ll;
+  const long long up = __shfl_up_sync(kFull, x, 1);
+  *total = sw[kListWarps - 1];
+  return before_warp + (lane > 0 ? up : 0ll);
+}
 
 // ---------------------------------------------------------------------------
 // Hashed plan: CTA `part` handles the ids whose hash partition is `part`.
@@ -349,8 +379,10 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   uint32_t* tkey = kinfo + kHashMaxN;    // table: id of the slot
   uint32_t* tcnt = tkey + kTableMax;     // table: occurrences of the id (run length)
   uint32_t* tbase = tcnt + kTableMax;    // table: descriptor of the run's first chunk
+  uint32_t* wcnt = tbase + kTableMax;    // table: the id's keys ranked so far
   __shared__ int wc[kHashItems * kHashWarps];
   __shared__ long long sw64[kHashWarps];
+  __shared__ int s_counts[3];   // long chunks, short chunks, long-run entries
   __shared__ int swi[kHashWarps];
   const int part = blockIdx.x;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -415,12 +447,14 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   for (int s = t; s < TS; s += kHashThreads) {
     tkey[s] = kEmptySlot;
     tcnt[s] = 0;
+    wcnt[s] = 0;
   }
   __syncthreads();
 
   // 3. the slot of every key: linear probing; there are at least as many slots as ids,
   // so every probe sequence ends within TS steps.  Within a warp only one lane per
-  // distinct id probes (a hot id would otherwise serialise on one slot).
+  // distinct id probes (a hot id would otherwise serialise on one slot) and adds the
+  // group's keys to the id's count.
   for (int i0 = warp * 32; i0 < m; i0 += kHashThreads) {
     const int i = i0 + lane;
     const bool valid = i < m;
@@ -439,6 +473,7 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
         }
         h = (h + 1) & static_cast<uint32_t>(TS - 1);
       }
+      atomicAdd(&tcnt[h], static_cast<uint32_t>(__popc(peers)));   // the id's run length
     }
     h = __shfl_sync(kFull, h, leader);
     // the key's rank among its group's keys of the same id, the group's last such key
@@ -450,8 +485,11 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   }
   __syncthreads();
 
-  // 4. ranks in position order: one warp carries the per-slot counts across the 32-key
-  // groups in order; each group's last key of an id adds the group's count
+  // 4 and 5 side by side.  Warp 0 gives every key its rank in position order: it carries
+  // the per-slot counts across the 32-key groups in order, each group's last key of an id
+  // adding the group's count.  Meanwhile the other warps list the runs (their lengths are
+  // the probe's counts): a scan over the table gives each run its first descriptor, and
+  // long runs also get their partial rows and their row of the long-run table.
   if (warp == 0) {
     uint32_t next = lane < m ? kinfo[lane] : 0u;
     for (int i0 = 0; i0 < m; i0 += 32) {
@@ -463,36 +501,38 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
       const int last = static_cast<int>((info >> kLastShift) & 31u);
       uint32_t prior = 0;
       if (valid && lane == last) {
-        prior = tcnt[s];
-        tcnt[s] = prior + ((info >> kGroupCntShift) & 31u) + 1u;
+        prior = wcnt[s];
+        wcnt[s] = prior + ((info >> kGroupCntShift) & 31u) + 1u;
       }
       __syncwarp();
       const uint32_t base = __shfl_sync(kFull, prior, last);
       if (valid) kinfo[i] = s | ((base + ((info >> kInRankShift) & 31u)) << kRankShift);
     }
-  }
-  __syncthreads();
-
-  // 5. runs: a scan over the table gives each run its first descriptor; long runs also
-  // get their partial rows and their row of the long-run table
-  long long cnt = 0;
-  for (int s = t; s < TS; s += kHashThreads) {
-    const int L = static_cast<int>(tcnt[s]);
-    if (L > kNrows) {
-      const int C = (L + kNrows - 1) / kNrows;
-      cnt += (static_cast<long long>(C) << kField) + fold_entries(C);
-    } else if (L > 0) {
-      cnt += 1ll << (2 * kField);
+  } else {
+    constexpr int NL = kListWarps * 32;
+    const int u = t - 32;
+    long long cnt = 0;
+    for (int s = u; s < TS; s += NL) {
+      const int L = static_cast<int>(tcnt[s]);
+      if (L > kNrows) {
+        const int C = (L + kNrows - 1) / kNrows;
+        cnt += (static_cast<long long>(C) << kField) + fold_entries(C);
+      } else if (L > 0) {
+        cnt += 1ll << (2 * kField);
+      }
     }
-  }
-  long long tot = 0;
-  const long long pre = block_exclusive_scan<kHashThreads, long long>(cnt, SumOp(), 0ll, sw64, &tot);
-  const int n_long = field_long(tot), n_short = field_short(tot), n_runs = field_runs(tot);
-  const int long_desc = S_b, short_desc = S_b + n_long;
-  const int partial_base = (2 * S_b) / 11 + part, run_base = S_b / 11 + S_b / 100 + part;
-  {
+    long long tot = 0;
+    const long long pre = list_warps_exclusive_sum(cnt, sw64, &tot);
+    const int n_long = field_long(tot);
+    if (u == 0) {
+      s_counts[0] = n_long;
+      s_counts[1] = field_short(tot);
+      s_counts[2] = field_runs(tot);
+    }
+    const int long_desc = S_b, short_desc = S_b + n_long;
+    const int partial_base = (2 * S_b) / 11 + part, run_base = S_b / 11 + S_b / 100 + part;
     int li = field_long(pre), si = field_short(pre), ri = field_runs(pre);
-    for (int s = t; s < TS; s += kHashThreads) {
+    for (int s = u; s < TS; s += NL) {
       const int L = static_cast<int>(tcnt[s]);
       if (L > kNrows) {
         const int C = (L + kNrows - 1) / kNrows;
@@ -513,6 +553,9 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
     }
   }
   __syncthreads();
+  const int n_long = s_counts[0], n_short = s_counts[1], n_runs = s_counts[2];
+  const int long_desc = S_b, short_desc = S_b + n_long;
+  const int partial_base = (2 * S_b) / 11 + part, run_base = S_b / 11 + S_b / 100 + part;
 
   // 6. every key writes its position into its chunk; the first key of a chunk also
   // writes the chunk's id, length, index in the run, partial row and the run's size
