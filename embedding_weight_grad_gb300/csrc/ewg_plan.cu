@@ -383,7 +383,8 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   __shared__ int wc[kHashItems * kHashWarps];
   __shared__ long long sw64[kHashWarps];
   __shared__ int s_counts[3];   // long chunks, short chunks, long-run entries
-  __shared__ int swi[kHashWarps];
+  __shared__ long long s_red;   // bad ids << 32 | tokens of lower partitions
+  __shared__ int s_m;           // keys of this partition
   const int part = blockIdx.x;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const uint32_t lt = (1u << lane) - 1u;
@@ -417,7 +418,41 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
     ballot[r] = __ballot_sync(kFull, mine);
     if (lane == 0) wc[r * kHashWarps + warp] = __popc(ballot[r]);
   }
-  const long long red = block_sum<kHashThreads>((static_cast<long long>(bad) << 32) | before, sw64);
+  // One pass of warp 0 over the warps' results gives the block's bad ids and tokens of
+  // lower partitions, and turns the (round, warp) key counts into offsets in that order
+  // (position order) and their total m.
+  {
+    long long bb = (static_cast<long long>(bad) << 32) | before;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) bb += __shfl_xor_sync(kFull, bb, o);
+    if (lane == 0) sw64[warp] = bb;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    static_assert(kHashWarps == 32 && kHashItems * kHashWarps == 8 * 32, "one lane per warp, 8 counts each");
+    long long tot = sw64[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
+    int v[8], sum = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int x = wc[8 * lane + j];
+      v[j] = sum;
+      sum += x;
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) wc[8 * lane + j] = v[j] + incl - sum;
+    if (lane == 31) s_m = incl;
+    if (lane == 0) s_red = tot;
+  }
+  __syncthreads();
+  const long long red = s_red;
   const int bad_total = static_cast<int>(red >> 32);
   const int S_b = static_cast<int>(red & 0xffffffffll);   // tokens of partitions < part
   if (bad_total) {
@@ -426,13 +461,7 @@ __global__ void __launch_bounds__(kHashThreads, 1) plan_hashed_kernel(PlanArgs a
   }
 
   // 2. this partition's keys, compacted in position order
-  int m = 0;
-  {
-    const int v = t < kHashItems * kHashWarps ? wc[t] : 0;
-    const int off = block_exclusive_scan<kHashThreads, int>(v, SumIntOp(), 0, swi, &m);
-    if (t < kHashItems * kHashWarps) wc[t] = off;
-    __syncthreads();
-  }
+  const int m = s_m;
 #pragma unroll
   for (int r = 0; r < kHashItems; ++r) {
     if ((ballot[r] >> lane) & 1u) {
