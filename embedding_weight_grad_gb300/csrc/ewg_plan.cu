@@ -230,10 +230,22 @@ struct Listing {
   // Writes the descriptors of the chunks that start in this thread's slots; `prefix`
   // is the packed count of the chunks and runs before this thread's slots.  sval: the
   // positions of slots s_begin .. s_begin + NT * ITEMS + NROWS - 1, staged in shared memory.
+  // Each warp's descriptors are contiguous in their list (long chunks, short chunks), so
+  // the warp builds them in its shared-memory stage (`wstage`, kEmitStage int4; `wmap`,
+  // kEmitMap ints) and writes each list's run of them with coalesced 16-byte stores: one
+  // thread's 64-byte descriptors written directly sit 256 bytes apart across the warp,
+  // a partial sector per lane.
+  static constexpr int kWarpDescs = 32 * ITEMS;        // descriptors of a warp, at most
+  static constexpr int kEmitStage = kWarpDescs * kChunkWords / 4;
+  static constexpr int kEmitMap = 2 * kWarpDescs;
   __device__ void emit(const PlanArgs& a, const uint32_t* sval, int n, int s_begin,
-                       long long prefix, const EmitBases& b) const {
+                       long long prefix, const EmitBases& b, int4* wstage, int* wmap) const {
     const int base = s_begin + threadIdx.x * ITEMS;
+    const int lane = static_cast<int>(threadIdx.x & 31);
     int si = field_short(prefix), li = field_long(prefix), ri = field_runs(prefix);
+    const int li0 = __shfl_sync(kFull, li, 0), si0 = __shfl_sync(kFull, si, 0);
+    int nd = 0;   // this thread's descriptors so far: part q of the nd-th sits at
+                  // wstage[(nd * 4 + q) * 32 + (lane ^ q)] (conflict-free both ways)
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int s = base + i;
@@ -245,21 +257,27 @@ struct Listing {
       const bool is_long = L > kNrows;
       const int desc = is_long ? b.long_desc + li : b.short_desc + si;
       const int prow = is_long ? b.partial + li : -1;
-      if (!checked(desc >= 0 && desc < a.chunk_cap && prow < a.partial_cap &&
-                       (!is_long || c != 0 || b.run + ri + fold_entries(C) <= a.run_cap),
-                   a.header))
-        continue;
-      int4* d = reinterpret_cast<int4*>(a.chunks + static_cast<long long>(desc) * kChunkWords);
+      const bool ok = checked(desc >= 0 && desc < a.chunk_cap && prow < a.partial_cap &&
+                                  (!is_long || c != 0 || b.run + ri + fold_entries(C) <= a.run_cap),
+                              a.header);
       int p[kNrows];
 #pragma unroll
       for (int k = 0; k < kNrows; ++k) {
         p[k] = k < len ? static_cast<int>(sval[s - s_begin + k]) : 0;
         if (!checked(p[k] >= 0 && p[k] < n, a.header)) p[k] = 0;
       }
-      d[0] = make_int4(p[0], p[1], p[2], p[3]);
-      d[1] = make_int4(p[4], p[5], p[6], p[7]);
-      d[2] = make_int4(p[8], p[9], static_cast<int>(key[i]), len | (c << 4));
-      d[3] = make_int4(prow, C, 0, 0);
+      wstage[(nd * 4 + 0) * 32 + (lane ^ 0)] = make_int4(p[0], p[1], p[2], p[3]);
+      wstage[(nd * 4 + 1) * 32 + (lane ^ 1)] = make_int4(p[4], p[5], p[6], p[7]);
+      wstage[(nd * 4 + 2) * 32 + (lane ^ 2)] = make_int4(p[8], p[9], static_cast<int>(key[i]), len | (c << 4));
+      wstage[(nd * 4 + 3) * 32 + (lane ^ 3)] = make_int4(prow, C, 0, 0);
+      // where the writer finds it: the descriptor's place in the warp's run of its list
+      wmap[is_long ? li - li0 : kWarpDescs + si - si0] = ok ? (lane | (nd << 5)) : -1;
+      ++nd;
+      if (!ok) {   // nothing written for it but its (skipped) place in the list
+        if (is_long) ++li;
+        else ++si;
+        continue;
+      }
       if (is_long) {
         if (c == 0) {
           const int split = fold_entries(C);
@@ -273,6 +291,19 @@ struct Listing {
       } else {
         ++si;
       }
+    }
+    __syncwarp();
+    const int nl = __shfl_sync(kFull, li, 31) - li0, ns = __shfl_sync(kFull, si, 31) - si0;
+    int4* const dst_long = reinterpret_cast<int4*>(a.chunks) + static_cast<long long>(b.long_desc + li0) * 4;
+    int4* const dst_short = reinterpret_cast<int4*>(a.chunks) + static_cast<long long>(b.short_desc + si0) * 4;
+    for (int q = lane; q < 4 * (nl + ns); q += 32) {
+      const int g = q >> 2, part = q & 3;
+      const bool lng = g < nl;
+      const int m = wmap[lng ? g : kWarpDescs + g - nl];
+      if (m < 0) continue;
+      const int4 v = wstage[((m >> 5) * 4 + part) * 32 + ((m & 31) ^ part)];
+      if (lng) dst_long[q] = v;
+      else dst_short[q - 4 * nl] = v;
     }
   }
 };
@@ -920,8 +951,14 @@ constexpr int kListItems = kTile / kListThreads;
 // Runs and chunks of the sorted keys, one tile per CTA (tiles in claim order).  The tile's
 // keys (with one slot on each side) and positions (with the NROWS - 1 slots after it) are
 // staged in shared memory by one coalesced load.
+using ListTile = Listing<kListThreads, kListItems>;
+// per warp: the descriptors it builds (transposed) and where its writers find them
+constexpr size_t kListDynSmem = static_cast<size_t>(kListThreads / 32) *
+                                (ListTile::kEmitStage * sizeof(int4) + ListTile::kEmitMap * sizeof(int));
+
 __global__ void __launch_bounds__(kListThreads) list_kernel(PlanArgs a, const uint32_t* keys,
                                                             const uint32_t* vals) {
+  extern __shared__ __align__(16) int4 emit_smem[];   // kListDynSmem
   __shared__ uint32_t skey[kTile + 2];
   __shared__ uint32_t sval[kTile + kNrows];
   __shared__ int swi[kListThreads / 32];
@@ -968,7 +1005,7 @@ __global__ void __launch_bounds__(kListThreads) list_kernel(PlanArgs a, const ui
   }
   int rs_seed, re_seed;
   tile_seeds(keys, a.n, s0, &rs_seed, &re_seed);
-  Listing<kListThreads, kListItems> L;
+  ListTile L;
   L.compute(skey, a.n, s0, rs_seed, re_seed, swi);
   long long tot = 0;
   const long long prefix = block_exclusive_scan<kListThreads, long long>(L.counts(a.n, s0, a.skip_key),
@@ -995,7 +1032,13 @@ __global__ void __launch_bounds__(kListThreads) list_kernel(PlanArgs a, const ui
   eb.short_desc = a.short_base + static_cast<int>(s_before[1]);
   eb.partial = static_cast<int>(s_before[0]);
   eb.run = static_cast<int>(s_before[2]);
-  L.emit(a, sval, a.n, s0, prefix, eb);
+  {
+    const int w = t >> 5;
+    int4* wstage = emit_smem + w * ListTile::kEmitStage;
+    int* wmap = reinterpret_cast<int*>(emit_smem + (kListThreads / 32) * ListTile::kEmitStage) +
+                w * ListTile::kEmitMap;
+    L.emit(a, sval, a.n, s0, prefix, eb, wstage, wmap);
+  }
   if (tile == a.tiles - 1 && t == 0) {
     write_tables(a, 0, static_cast<int>(s_before[0] + s_own[0]), 0, static_cast<int>(s_before[1] + s_own[1]),
                  a.short_base, static_cast<int>(s_before[2] + s_own[2]), 0);
@@ -1007,8 +1050,12 @@ __global__ void __launch_bounds__(kListThreads) list_kernel(PlanArgs a, const ui
 
 cudaError_t prepare_kernels() {
   static_assert(kHashSmem <= 227 * 1024, "hashed plan must fit in shared memory");
-  return cudaFuncSetAttribute(plan_hashed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(kHashSmem));
+  static_assert(kListDynSmem + 24 * 1024 <= 227 * 1024, "listing stages must fit in shared memory");
+  cudaError_t e = cudaFuncSetAttribute(plan_hashed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(kHashSmem));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(list_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kListDynSmem));
 }
 
 namespace {
@@ -1058,7 +1105,7 @@ cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
     ks = nk;
     vs = nv;
   }
-  if (e == cudaSuccess) e = launch_pdl(list_kernel, tiles, kListThreads, 0, stream, a, ks, vs);
+  if (e == cudaSuccess) e = launch_pdl(list_kernel, tiles, kListThreads, kListDynSmem, stream, a, ks, vs);
   return e;
 }
 
